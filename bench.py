@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA hot path (indexer -> top-k -> sparse MLA attention) on B300.
+
+Default run (N=1): one step = the whole forward of one 128K-token prefill sequence
+(L=131072, H_I=64, d_I=128 FP8, k=2048, H=128, 576-d bf16 latent), inputs resident in HBM.
+`value` is prefill tokens/s; the decode figure (query tokens/s, B=32 mixed contexts up to
+128K) rides along under "decode".  Prints ONE JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own 128K sequence (weak scaling, no collective on the
+data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "DSA prefill tokens/s & decode query-tok/s at 128K ctx; % of FP8/HBM roofline"
+L2_BYTES = 126 * 1024 * 1024
+
+
+# ------------------------------------------------------------------------------------ utils
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "-i", str(index),
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.seek(0)
+        rows = [r.split(", ") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip() == "Active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        rank, local = dist.get_rank(), int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        return dist, rank, ws, local
+    return None, 0, 1, 0
+
+
+def _max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(dist):
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------------------------ work counts
+
+def prefill_work(L, H_I, H, k):
+    causal = L * (L + 1) // 2
+    sel = sum(min(t + 1, k) for t in range(0, min(L, k))) + max(0, L - k) * k
+    return dict(
+        indexer_flop=2.0 * H_I * 128 * causal,
+        topk_bytes=4.0 * causal + 4.0 * k * L,
+        attn_flop=2.0 * H * (576 + 512) * sel,
+        attn_bytes=L * H * 576 * 2.0 + L * H * 512 * 2.0 + 4.0 * k * L + 576 * 2.0 * L,
+    )
+
+
+def decode_work(lens, H_I, H, k):
+    n = float(sum(lens))
+    sel = float(sum(min(k, x) for x in lens))
+    B = len(lens)
+    return dict(
+        indexer_bytes=n * (128 + 4) + 4.0 * n + B * H_I * (128 + 8),
+        topk_bytes=4.0 * n + 4.0 * k * B,
+        attn_bytes=sel * 1152 + B * H * 576 * 2.0 + B * H * 512 * 2.0 + 4.0 * k * B,
+        attn_flop=2.0 * H * (576 + 512) * sel,
+    )
+
+
+# ------------------------------------------------------------------------------------ our arm
+
+class PrefillRunner:
+    """One 128K prefill step through the C ABI, stage by stage, with CUDA events per launch
+    on the launching stream.  The launches are exactly those dsa_forward makes (same chunking)."""
+
+    def __init__(self, dsa, d, cfg, chunk):
+        self.dsa, self.d, self.cfg, self.chunk = dsa, d, cfg, chunk
+        L = cfg.L
+        ld = (L + 3) // 4 * 4
+        self.scores = torch.empty((chunk, ld), dtype=torch.float32, device="cuda")
+        self.idx = torch.empty((L, cfg.k), dtype=torch.int32, device="cuda")
+        self.out = torch.empty((L, cfg.H, 512), dtype=torch.bfloat16, device="cuda")
+        self.lse = torch.empty((L, cfg.H), dtype=torch.float32, device="cuda")
+        self.n_chunks = (L + chunk - 1) // chunk
+        self.launches = 2 * self.n_chunks + 1
+
+    def step(self, events=None):
+        dsa, d, cfg = self.dsa, self.d, self.cfg
+        ev = events
+        for c in range(self.n_chunks):
+            r0 = c * self.chunk
+            r1 = min(cfg.L, r0 + self.chunk)
+            sc = self.scores[: r1 - r0]
+            if ev is not None:
+                ev["index"].append(_rec())
+            dsa.index(d["q8"][r0:r1], d["q_scale"][r0:r1], d["w"][r0:r1], d["k8"], d["k_scale"], q_pos0=r0,
+                      scores=sc)
+            if ev is not None:
+                ev["index"].append(_rec())
+                ev["topk"].append(_rec())
+            dsa.topk(sc, cfg.k, q_pos0=r0, n_cols=cfg.L, idx=self.idx[r0:r1])
+            if ev is not None:
+                ev["topk"].append(_rec())
+        if ev is not None:
+            ev["attn"].append(_rec())
+        dsa.sparse_attn(d["q"], d["kv"], self.idx, cfg.scale, out=self.out, lse=self.lse)
+        if ev is not None:
+            ev["attn"].append(_rec())
+
+
+def _rec():
+    e = torch.cuda.Event(enable_timing=True)
+    e.record()
+    return e
+
+
+def _pairs_ms(lst):
+    return sum(a.elapsed_time(b) for a, b in zip(lst[0::2], lst[1::2]))
+
+
+def run_ours(args, dist, rank, ws):
+    import synth
+    from sparse_attention_30_b300 import build
+    build.build()
+    import sparse_attention_30_b300 as dsa
+
+    peaks = _peaks()
+    cfg = synth.config(4)
+    if rank:
+        cfg = synth.config(4, seed=cfg.seed + 1000 * rank)
+    d = synth.prefill_inputs(cfg, device="cuda")
+    runner = PrefillRunner(dsa, d, cfg, args.chunk)
+
+    for _ in range(args.warmup):
+        runner.step()
+    st = dsa.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    ev = {"index": [], "topk": [], "attn": []}
+    _barrier(dist)
+    t0, t1 = _rec(), None
+    for _ in range(args.steps):
+        runner.step(ev)
+    t1 = _rec()
+    _barrier(dist)
+    clk = clocks.stop() if clocks else None
+    total_ms = _max_over_ranks(dist, t0.elapsed_time(t1))
+    st = dsa.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the timed region")
+    ms_step = total_ms / args.steps
+    tokens = cfg.L * ws * args.steps
+    value = tokens / (total_ms / 1e3)
+
+    # per-kernel rooflines (algorithmic work / summed launch time over the timed region)
+    w = prefill_work(cfg.L, cfg.H_I, cfg.H, cfg.k)
+    t_index = _pairs_ms(ev["index"]) / args.steps
+    t_topk = _pairs_ms(ev["topk"]) / args.steps
+    t_attn = _pairs_ms(ev["attn"]) / args.steps
+    fp8_peak = 2.0 * peaks["bf16_sus"]
+    bf16_peak = peaks["bf16_sus"]
+    kern = {
+        "indexer": dict(bound="tensor", achieved=w["indexer_flop"] / (t_index * 1e-3) / 1e12, peak=fp8_peak,
+                        unit="TFLOP/s", ms=t_index, launches=runner.n_chunks),
+        "topk": dict(bound="hbm", achieved=w["topk_bytes"] / (t_topk * 1e-3) / 1e9, peak=peaks["hbm"],
+                     unit="GB/s", ms=t_topk, launches=runner.n_chunks),
+        "sparse_attn": dict(bound="tensor", achieved=w["attn_flop"] / (t_attn * 1e-3) / 1e12, peak=bf16_peak,
+                            unit="TFLOP/s", ms=t_attn, launches=1),
+    }
+    for v in kern.values():
+        v["frac"] = v["achieved"] / v["peak"]
+    dom_name = max(kern, key=lambda n: kern[n]["ms"])
+    dom = kern[dom_name]
+    roofline = {"kernel": dom_name, "bound": dom["bound"], "achieved": round(dom["achieved"], 2),
+                "peak": dom["peak"], "unit": dom["unit"], "frac": round(dom["frac"], 4), "traffic": None,
+                "peak_source": f"{peaks['src']} (sustained; FP8 = 2 x bf16)" if dom["unit"] == "TFLOP/s"
+                else f"{peaks['src']} copy bandwidth"}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 indexer / bf16 attention (fp32 accum)",
+            "data": "synthetic (seeded; shapes and distributions of the 128K prefill workload)",
+            "config": {"workload": "prefill L=131072 (128K), H_I=64, d_I=128, k=2048, H=128, D=576/512",
+                       "seq_len": cfg.L, "global_batch": ws, "chunk_rows": args.chunk,
+                       "l2": "inputs larger than L2 (Q 19.3 GB, O 17.2 GB per step)", "parallelism": f"dp{ws}"},
+            "roofline": roofline,
+            "kernels": {n: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                        for n, v in kern.items()},
+            "gpu_launches": runner.launches * args.steps,
+            "clocks": clk}
+
+    if not args.no_decode:
+        line["decode"] = bench_decode(dsa, synth, args, peaks)
+    if not args.no_e2e:
+        line["e2e"] = bench_e2e(dsa, d, cfg, args)
+    del d, runner
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_seconds)
+    return line
+
+
+def bench_decode(dsa, synth, args, peaks):
+    """Decode step (B=32, contexts ~U[8192,131072]) through dsa_forward; L2 flushed between steps."""
+    cfg = synth.config(5)
+    d = synth.decode_inputs(cfg, device="cuda")
+    lens = d["seq_lens"].cpu().tolist()
+    max_len = max(lens)
+    f = dsa.Forward.decode(d, cfg.k, cfg.scale, max_len)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    for _ in range(max(3, args.warmup)):
+        f()
+    times = []
+    for _ in range(max(10, args.steps)):
+        flush.fill_(1.0)
+        a = _rec()
+        f()
+        b = _rec()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    st = dsa.device_status()
+    if st != 0:
+        raise RuntimeError(f"decode status {st}")
+    ms = float(np.median(times))
+    w = decode_work(lens, cfg.H_I, cfg.H, cfg.k)
+    tot_bytes = w["indexer_bytes"] + w["topk_bytes"] + w["attn_bytes"]
+    return {"metric": "decode query-tok/s", "value": round(cfg.B / (ms * 1e-3), 1), "unit": "query-tok/s",
+            "ms_per_step": round(ms, 4), "workload": "mixed decode B=32, ctx~U[8192,131072], k=2048, H=128",
+            "algorithmic_bytes": tot_bytes, "hbm_frac_of_step": round(tot_bytes / (ms * 1e-3) / 1e9 / peaks["hbm"], 4),
+            "l2": "flushed between steps (252 MB write)"}
+
+
+def bench_e2e(dsa, d, cfg, args):
+    """Same prefill step through dsa_forward with inputs and output in pinned host memory:
+    per step H2D of every input, the forward, and D2H of the attention output."""
+    names = ["q8", "q_scale", "w", "k8", "k_scale", "q", "kv"]
+    need = sum(d[n].numel() * d[n].element_size() for n in names) + cfg.L * cfg.H * 512 * 2
+    try:
+        avail = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError):
+        avail = 0
+    if avail < 1.5 * need:
+        return {"value": None, "unit": "tokens/s", "skipped": f"host memory {avail / 2**30:.0f} GiB < 1.5 x {need / 2**30:.0f} GiB"}
+    host = {n: torch.empty_like(d[n], device="cpu").pin_memory() for n in names}
+    for n in names:
+        host[n].copy_(d[n])
+    host_out = torch.empty((cfg.L, cfg.H, 512), dtype=torch.bfloat16).pin_memory()
+    dev = {n: torch.empty_like(d[n]) for n in names}
+    f = dsa.Forward.prefill(dev, cfg.k, cfg.scale, chunk_rows=args.chunk)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = host_out.numel() * 2
+
+    def step():
+        for n in names:
+            dev[n].copy_(host[n], non_blocking=True)
+        f()
+        host_out.copy_(f.out, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    n_steps = max(2, min(args.steps, 3))
+    a = _rec()
+    for _ in range(n_steps):
+        step()
+    b = _rec()
+    b.synchronize()
+    ms = a.elapsed_time(b) / n_steps
+    st = dsa.device_status()
+    if st != 0:
+        raise RuntimeError(f"e2e status {st}")
+    return {"value": round(cfg.L / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 2),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_steps,
+            "path": "dsa_forward (C ABI) with pinned host buffers"}
+
+
+# ------------------------------------------------------------------------------------ oracle arm
+
+def _oracle_rows_rate(cfg, d, rows):
+    """Times the float64 oracle on the given prefill rows; returns (rows/s, seconds)."""
+    import oracle
+    keys = {n: d[n].cpu() for n in ("k8", "k_scale", "kv")}
+    t_sum = 0.0
+    for t in rows:
+        row = dict(keys, **{n: {t: d[n][t].cpu()} for n in ("q8", "q_scale", "w", "q")})
+        t0 = time.perf_counter()
+        oracle.prefill_row(row, int(t), cfg.k, cfg.scale)
+        t_sum += time.perf_counter() - t0
+    return len(rows) / t_sum, t_sum
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, budget_s=12.0, d=None):
+    """Oracle tokens/s on a stratified sample of rows of the same 128K workload."""
+    import synth
+    if d is None:
+        d = synth.prefill_inputs(cfg, device="cuda")
+    rng = np.random.default_rng(0)
+    rows, spent, n = [], 0.0, 0
+    strata = 64
+    while spent < budget_s and n < 4096:
+        s = n % strata
+        rows_s = [int((s + rng.random()) * cfg.L / strata)]
+        _, dt = _oracle_rows_rate(cfg, d, rows_s)
+        spent += dt
+        rows += rows_s
+        n += 1
+    rate = len(rows) / spent
+    return {"value": round(rate, 3), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} prefill rows of the 128K workload, stratified over positions "
+                      f"(float64 NumPy oracle: scores, full sort, attention), {spent:.1f} s"}
+
+
+def run_reference(args, dist, rank, ws):
+    """The oracle as the reference arm: each step is a bounded sample of the 128K workload."""
+    import synth
+    if rank != 0:
+        return None
+    cfg = synth.config(4)
+    d = synth.prefill_inputs(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+    rng = np.random.default_rng(1)
+    per_step = 4
+    for _ in range(args.warmup):
+        _oracle_rows_rate(cfg, d, [int(rng.integers(0, cfg.L))])
+    total_rows, total_s = 0, 0.0
+    for i in range(args.steps):
+        rows = [int((j + rng.random()) * cfg.L / per_step) for j in range(per_step)]
+        _, dt = _oracle_rows_rate(cfg, d, rows)
+        total_rows += len(rows)
+        total_s += dt
+    value = total_rows / total_s
+    cores = _blas_threads()
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; the 128K prefill workload)",
+            "config": {"workload": "prefill L=131072 (128K), H_I=64, d_I=128, k=2048, H=128, D=576/512",
+                       "seq_len": cfg.L, "global_batch": 1},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} stratified rows per step, {total_rows} rows"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--chunk", type=int, default=8192)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-decode", action="store_true")
+    args = p.parse_args()
+    args.warmup = max(3, args.warmup)
+    dist, rank, ws, _ = _dist()
+    line = run_reference(args, dist, rank, ws) if args.impl == "reference" else run_ours(args, dist, rank, ws)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+/*
+ * dsa.h — C ABI of libdsa.so: DeepSeek Sparse Attention (DSA) forward on one
+ * NVIDIA B300 (sm_103a).
+ *
+ * The method (freezhihu.org/question/1978819912970555965, §2.1–§2.2):
+ *   1. lightning indexer   I[t,s] = sum_j w[t,j] * ReLU(q^I[t,j] . k^I[s])   (§2.1.1 equation)
+ *      over the preceding tokens s <= t, with FP8 indexer inputs (§2.1.1);
+ *   2. fine-grained token selection: the k positions with the largest I[t,s] (§2.1.2);
+ *   3. attention of token t over only the selected latent rows c_s (§2.1.2 output
+ *      equation), in the MQA mode of MLA: each 576-dim latent row is shared by all
+ *      query heads and its first 512 dims are the value (§2.2).
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns every
+ *     buffer and the library never allocates device memory.
+ *   - Tensors are dense, row-major, contiguous unless a leading dimension is given.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - FP8 tensors are e4m3 ("fn": no infinities) bytes; every FP8 scale is a positive,
+ *     finite fp32 (the score uses ReLU(sq*sk*x) = sq*sk*ReLU(x), which needs sq, sk > 0).
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).  Argument
+ *     errors are detected on the host and returned before anything is launched;
+ *     a failed launch returns DSA_ERR_CUDA.  Device-side faults the kernels detect
+ *     themselves (a wait that timed out, an index out of range) are recorded in a
+ *     per-device status word that dsa_device_status() returns and clears.
+ *   - No C++ exception crosses this boundary.  The functions are thread-safe as long
+ *     as calls that share output buffers are ordered by the caller.
+ *   - Pointers to FP8 / bf16 row data must be 16-byte aligned (the kernels move rows
+ *     with 16-byte copies and the tensor-memory accelerator).
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,    /* a null pointer, a bad size or a misaligned pointer */
+  DSA_ERR_UNSUPPORTED = 2,    /* a shape the kernels are not built for (e.g. d_I != 128) */
+  DSA_ERR_WORKSPACE = 3,      /* the workspace is missing or smaller than required */
+  DSA_ERR_CUDA = 4,           /* a CUDA runtime call or a kernel launch failed */
+  DSA_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up on a bounded wait (see dsa_device_status) */
+  DSA_ERR_DEVICE_RANGE = 6    /* a kernel met an index or page number out of range and skipped it */
+} dsa_status_t;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* dsa_status_string(dsa_status_t status);
+
+/* Library ABI version: (major << 16) | minor. */
+int dsa_version(void);
+
+/*
+ * dsa_index — lightning-indexer scores for a block of prefill query rows
+ * (freezhihu.org/question/1978819912970555965 §2.1.1, indexer equation).
+ *
+ * Row t (0 <= t < T) is the query at absolute position q_pos0 + t; keys are the
+ * positions 0 .. S-1.  For every s <= min(q_pos0 + t, S - 1) it writes
+ *     scores[t * ld + s] = k_scale[s] * sum_j (w[t,j] * q_scale[t,j]) * ReLU(q8[t,j,:] . k8[s,:])
+ * with the FP8 products accumulated in fp32 on the tensor cores and the head sum in fp32.
+ * Entries with s > q_pos0 + t are not written.
+ *
+ *   q8       [T, H_I, 128]  e4m3, 16-byte aligned
+ *   q_scale  [T, H_I]       fp32 per (token, head) dequantisation scale
+ *   w        [T, H_I]       fp32 head weights w^I
+ *   k8       [S, 128]       e4m3, 16-byte aligned
+ *   k_scale  [S]            fp32 per-key scale
+ *   scores   [T, ld]        fp32 output, ld >= min(S, q_pos0 + T), ld % 4 == 0, 16-byte aligned
+ *   H_I must be a power of two in [1, 128]; T, S >= 1 (T = 0 is a no-op); q_pos0 >= 0.
+ */
+dsa_status_t dsa_index(const uint8_t* q8, const float* q_scale, const float* w,
+                       const uint8_t* k8, const float* k_scale,
+                       int T, int S, int H_I, int64_t q_pos0,
+                       float* scores, int64_t ld, dsa_stream_t stream);
+
+/*
+ * dsa_index_paged — indexer scores of one new query token per sequence against a
+ * paged FP8 key cache (decode).  Sequence b holds seq_lens[b] tokens, the new one
+ * included (it sits at position seq_lens[b] - 1 and scores itself too).  Logical
+ * position p of sequence b lives in page block_table[b * bt_stride + p / page_size],
+ * slot p % page_size.  Writes scores[b * ld + p] for 0 <= p < seq_lens[b].
+ *
+ *   q8 [B, H_I, 128], q_scale [B, H_I], w [B, H_I]   as in dsa_index, one token per sequence
+ *   k8_cache      [n_pages, page_size, 128] e4m3, 16-byte aligned
+ *   k_scale_cache [n_pages, page_size]      fp32
+ *   block_table   [B, bt_stride] int32 page numbers (entries past a sequence's last page are not read)
+ *   seq_lens      [B] int32, each in [1, max_seq_len]
+ *   scores        [B, ld] fp32, ld >= max_seq_len, ld % 4 == 0
+ *   page_size must divide 128 and be a multiple of 8; n_pages bounds the page numbers
+ *   (an out-of-range page number is skipped and reported as DSA_ERR_DEVICE_RANGE).
+ */
+dsa_status_t dsa_index_paged(const uint8_t* q8, const float* q_scale, const float* w,
+                             const uint8_t* k8_cache, const float* k_scale_cache, int64_t n_pages,
+                             const int32_t* block_table, int64_t bt_stride,
+                             const int32_t* seq_lens, int B, int H_I, int page_size, int max_seq_len,
+                             float* scores, int64_t ld, dsa_stream_t stream);
+
+/*
+ * dsa_topk — fine-grained token selection
+ * (freezhihu.org/question/1978819912970555965 §2.1.2; k = 2048 in §2.3.2).
+ *
+ * For each row t it selects the min(k, n_t) positions with the largest scores among
+ * scores[t * ld + 0 .. n_t - 1], where n_t = row_lens[t] if row_lens is not NULL,
+ * else min(n_cols, q_pos0 + t + 1) (the causal prefix of a prefill row).
+ * idx[t * k + i] receives the selected positions in slots 0 .. min(k, n_t) - 1 (in no
+ * particular order) and -1 in the remaining slots.  Equal scores at the boundary are
+ * broken arbitrarily; selection compares fp32 scores exactly (order-preserving integer
+ * keys), so NaN scores are not supported.
+ *
+ *   scores [T, ld] fp32 (16-byte aligned, ld % 4 == 0), idx [T, k] int32,
+ *   row_lens [T] int32 or NULL, 1 <= k <= 65536, every n_t <= ld.
+ */
+dsa_status_t dsa_topk(const float* scores, int64_t ld, int T, const int32_t* row_lens,
+                      int64_t n_cols, int64_t q_pos0, int k, int32_t* idx, dsa_stream_t stream);
+
+/*
+ * dsa_sparse_attn — MQA-mode MLA attention over the selected latent rows
+ * (freezhihu.org/question/1978819912970555965 §2.1.2 output equation, §2.2).
+ *
+ * For every row t and head h:
+ *     o[t,h,:] = sum_{s in S_t} softmax_s(scale * q[t,h,:] . c_s) * c_s[0:512]
+ * where S_t = { idx[t*k + i] : idx[t*k + i] >= 0 } (valid slots must come first) and
+ * c_s is latent row s: kv[s * 576 ...] if block_table is NULL, else slot s % page_size
+ * of page block_table[t * bt_stride + s / page_size] in kv viewed as
+ * [n_pages, page_size, 576].  QK^T and PV run on the tensor cores with bf16 inputs
+ * and fp32 accumulation; the softmax is in fp32.  A row with no valid slot yields
+ * zeros and lse = -inf.
+ *
+ *   q   [T, H, 576] bf16, 16-byte aligned, 1 <= H <= 128
+ *   kv  [n_kv_rows, 576] bf16 (n_kv_rows = n_pages * page_size when paged), 16-byte aligned
+ *   block_table [T, bt_stride] int32 (bt_stride >= 1) or NULL; page_size >= 1 when paged
+ *   idx [T, k] int32 (positions; an index >= n_kv_rows, a position whose page index is
+ *       >= bt_stride, or a page number out of range is treated as an empty slot and
+ *       reported as DSA_ERR_DEVICE_RANGE)
+ *   out [T, H, 512] bf16, 16-byte aligned
+ *   lse [T, H] fp32 natural-log sum-exp of the scaled logits, or NULL
+ */
+dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows,
+                             const int32_t* block_table, int64_t bt_stride, int page_size,
+                             const int32_t* idx, int T, int H, int k, float scale,
+                             uint16_t* out, float* lse, dsa_stream_t stream);
+
+/* Forward modes. */
+enum { DSA_MODE_PREFILL = 0, DSA_MODE_DECODE = 1 };
+
+/*
+ * Arguments of the fused forward (indexer -> top-k -> sparse attention).
+ *
+ * PREFILL: one sequence with S keys (positions 0 .. S-1) and T query rows at positions
+ *   q_pos0 .. q_pos0 + T - 1 (q_pos0 + T <= S).  q8/q_scale/w/q hold the T query rows,
+ *   k8 [S,128] / k_scale [S] / kv [S,576] the keys.  The library scores the rows in
+ *   chunks of chunk_rows (0 = library choice) so the fp32 score block stays bounded.
+ * DECODE: B sequences, one new token each, with paged caches k8 [n_pages,page,128],
+ *   k_scale [n_pages,page], kv [n_pages,page,576], block_table [B, bt_stride], seq_lens [B]
+ *   (each in [1, max_seq_len]); q8/q_scale/w/q hold the B query tokens.
+ *
+ * Outputs: out [rows, H, 512] bf16; lse [rows, H] fp32 or NULL; idx [rows, k] int32 or
+ * NULL (when NULL the selection lives in the workspace only).
+ */
+typedef struct {
+  int mode;           /* DSA_MODE_PREFILL or DSA_MODE_DECODE */
+  int H_I;            /* indexer heads (power of two, 1..128) */
+  int H;              /* attention heads (1..128) */
+  int k;              /* tokens selected per query (1..65536) */
+  float scale;        /* softmax scale */
+  /* prefill */
+  int T;
+  int S;
+  int64_t q_pos0;
+  int chunk_rows;
+  /* decode */
+  int B;
+  int page_size;
+  int64_t n_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+  int max_seq_len;
+  /* inputs */
+  const uint8_t* q8;
+  const float* q_scale;
+  const float* w;
+  const uint8_t* k8;
+  const float* k_scale;
+  const uint16_t* q;
+  const uint16_t* kv;
+  /* outputs */
+  uint16_t* out;
+  float* lse;
+  int32_t* idx;
+} dsa_forward_args;
+
+/* Bytes of device workspace dsa_forward needs for these arguments (0 on invalid args). */
+size_t dsa_forward_workspace_size(const dsa_forward_args* args);
+
+/*
+ * dsa_forward — the whole hot path: scores (dsa_index / dsa_index_paged), selection
+ * (dsa_topk) and attention (dsa_sparse_attn), asynchronously on `stream`.
+ * `ws` is a caller-owned device buffer of at least dsa_forward_workspace_size(args)
+ * bytes, 256-byte aligned; it holds the fp32 score block and the selection.
+ */
+dsa_status_t dsa_forward(const dsa_forward_args* args, void* ws, size_t ws_bytes,
+                         dsa_stream_t stream);
+
+/*
+ * dsa_device_status — synchronises `stream`, then returns and clears the status word
+ * the kernels write on the current device (DSA_OK if nothing was recorded).
+ * Returns DSA_ERR_CUDA if the synchronisation itself fails.
+ */
+dsa_status_t dsa_device_status(dsa_stream_t stream);
+
+/*
+ * dsa_selftest_wait_timeout — launches one block that waits on a barrier nobody
+ * arrives at, with a limit of timeout_us microseconds; the kernel then records
+ * DSA_ERR_DEVICE_TIMEOUT and returns.  Used to test the bounded-wait path without a
+ * hang.  Follow with dsa_device_status().
+ */
+dsa_status_t dsa_selftest_wait_timeout(int timeout_us, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

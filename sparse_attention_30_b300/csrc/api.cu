@@ -1,0 +1,320 @@
+// C-ABI entry points of libdsa.so (declared in include/dsa.h): argument checks on the
+// host, kernel launches on the caller's stream, the chunked forward driver, and the
+// per-device status word the kernels report into.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "dsa_internal.h"
+#include "dsa_ptx.cuh"
+
+namespace dsa {
+
+__device__ int g_status;  // per-device: DSA_OK or the first device-side error recorded
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+std::mutex g_mu;
+
+// Address of this device's status word (looked up once per device).
+int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+__global__ void wait_timeout_kernel(int* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_addr(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  // nobody arrives: the bounded wait must give up, record the timeout and return
+  ptx::mbar_wait(ptx::smem_addr(&bar), 0, &abort_flag, status, limit_ns);
+  __syncthreads();
+}
+
+}  // namespace
+
+bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                       uint32_t box_rows) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, elem,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+namespace {
+
+dsa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+dsa_status_t check_index_args(const uint8_t* q8, const float* q_scale, const float* w, const uint8_t* k8,
+                              const float* k_scale, int T, int S, int H_I, int64_t q_pos0, const float* scores,
+                              int64_t ld) {
+  if (T < 0 || S < 1 || q_pos0 < 0) return DSA_ERR_INVALID_ARG;
+  if (!q8 || !q_scale || !w || !k8 || !k_scale || !scores) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(scores)) return DSA_ERR_INVALID_ARG;
+  if (ld % 4 != 0 || ld < std::min<int64_t>(S, q_pos0 + T)) return DSA_ERR_INVALID_ARG;
+  if (!pow2(H_I) || H_I > 128) return DSA_ERR_INVALID_ARG;
+  if (!indexer_supported_heads(H_I, false)) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(T) * H_I > (1ll << 31) - 1 || q_pos0 + T > (1ll << 31) - 1) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+dsa_status_t check_paged_index_args(const uint8_t* q8, const float* q_scale, const float* w, const uint8_t* k8c,
+                                    const float* ksc, int64_t n_pages, const int32_t* bt, int64_t bt_stride,
+                                    const int32_t* lens, int B, int H_I, int page, int max_len, const float* scores,
+                                    int64_t ld) {
+  if (B < 0 || n_pages < 1 || max_len < 1 || bt_stride < 1) return DSA_ERR_INVALID_ARG;
+  if (!q8 || !q_scale || !w || !k8c || !ksc || !bt || !lens || !scores) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8c) || !aligned16(scores)) return DSA_ERR_INVALID_ARG;
+  if (ld % 4 != 0 || ld < max_len) return DSA_ERR_INVALID_ARG;
+  if (page < 8 || page > 128 || 128 % page != 0) return DSA_ERR_INVALID_ARG;
+  if (bt_stride < (max_len + page - 1) / page) return DSA_ERR_INVALID_ARG;
+  if (!pow2(H_I) || H_I > 128) return DSA_ERR_INVALID_ARG;
+  if (!indexer_supported_heads(H_I, true)) return DSA_ERR_UNSUPPORTED;
+  if (n_pages * page > (1ll << 31) - 1) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+dsa_status_t check_topk_args(const float* scores, int64_t ld, int T, int64_t n_cols, int64_t q_pos0, int k,
+                             const int32_t* idx, const int32_t* row_lens) {
+  if (T < 0 || k < 1 || k > 65536 || q_pos0 < 0) return DSA_ERR_INVALID_ARG;
+  if (!scores || !idx) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(scores) || ld % 4 != 0 || ld < 1) return DSA_ERR_INVALID_ARG;
+  if (!row_lens && (n_cols < 1 || n_cols > ld)) return DSA_ERR_INVALID_ARG;
+  if (ld > (1ll << 31) - 1) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+dsa_status_t check_attn_args(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* bt,
+                             int64_t bt_stride, int page, const int32_t* idx, int T, int H, int k,
+                             const uint16_t* out) {
+  if (T < 0 || H < 1 || k < 1 || k > 65536 || n_kv_rows < 1) return DSA_ERR_INVALID_ARG;
+  if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+  if (bt && (page < 1 || bt_stride < 1)) return DSA_ERR_INVALID_ARG;
+  if (H > 128) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+// Workspace layout of dsa_forward: [scores block (fp32)] [selection (int32), if not caller-owned]
+struct FwdPlan {
+  int rows;          // query rows in total
+  int chunk;         // rows scored per indexer / top-k launch
+  int64_t ld;        // score row pitch (floats)
+  size_t scores_bytes, idx_bytes, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+dsa_status_t plan_forward(const dsa_forward_args* a, FwdPlan* p) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  if (a->H_I < 1 || a->H < 1 || a->k < 1 || a->k > 65536) return DSA_ERR_INVALID_ARG;
+  if (a->mode == DSA_MODE_PREFILL) {
+    if (a->T < 0 || a->S < 1 || a->q_pos0 < 0 || a->q_pos0 + a->T > a->S) return DSA_ERR_INVALID_ARG;
+    p->rows = a->T;
+    p->ld = (static_cast<int64_t>(a->S) + 3) & ~3ll;
+    int chunk = a->chunk_rows > 0 ? a->chunk_rows : 0;
+    if (chunk == 0) {
+      // keep the fp32 score block near 1 GiB
+      const int64_t c = (1ll << 28) / p->ld;
+      chunk = static_cast<int>(std::max<int64_t>(256, std::min<int64_t>(c, 8192)));
+    }
+    p->chunk = std::max(1, std::min(chunk, std::max(1, a->T)));
+  } else if (a->mode == DSA_MODE_DECODE) {
+    if (a->B < 0 || a->max_seq_len < 1) return DSA_ERR_INVALID_ARG;
+    p->rows = a->B;
+    p->ld = (static_cast<int64_t>(a->max_seq_len) + 3) & ~3ll;
+    p->chunk = std::max(1, a->B);
+  } else {
+    return DSA_ERR_INVALID_ARG;
+  }
+  p->scores_bytes = align256(static_cast<size_t>(p->chunk) * p->ld * sizeof(float));
+  p->idx_bytes = a->idx ? 0 : align256(static_cast<size_t>(std::max(1, p->rows)) * a->k * sizeof(int32_t));
+  p->total = p->scores_bytes + p->idx_bytes;
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(dsa_status_t s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE_TIMEOUT: return "DSA_ERR_DEVICE_TIMEOUT";
+    case DSA_ERR_DEVICE_RANGE: return "DSA_ERR_DEVICE_RANGE";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+int dsa_version(void) { return (1 << 16) | 0; }
+
+dsa_status_t dsa_index(const uint8_t* q8, const float* q_scale, const float* w, const uint8_t* k8,
+                       const float* k_scale, int T, int S, int H_I, int64_t q_pos0, float* scores, int64_t ld,
+                       dsa_stream_t stream) {
+  dsa_status_t st = check_index_args(q8, q_scale, w, k8, k_scale, T, S, H_I, q_pos0, scores, ld);
+  if (st != DSA_OK || T == 0) return st;
+  int* status = status_ptr();
+  if (!status) return DSA_ERR_CUDA;
+  IndexerArgs a{};
+  a.q_scale = q_scale; a.w = w; a.k_scale = k_scale;
+  a.scores = scores; a.ld = ld; a.rows = T; a.S = S; a.q_pos0 = q_pos0;
+  a.status = status; a.limit_ns = kWaitLimitNs;
+  const int max_keys = static_cast<int>(std::min<int64_t>(S, q_pos0 + T));
+  return from_cuda(launch_indexer(q8, k8, S, H_I, false, max_keys, a, stream));
+}
+
+dsa_status_t dsa_index_paged(const uint8_t* q8, const float* q_scale, const float* w, const uint8_t* k8_cache,
+                             const float* k_scale_cache, int64_t n_pages, const int32_t* block_table,
+                             int64_t bt_stride, const int32_t* seq_lens, int B, int H_I, int page_size,
+                             int max_seq_len, float* scores, int64_t ld, dsa_stream_t stream) {
+  dsa_status_t st = check_paged_index_args(q8, q_scale, w, k8_cache, k_scale_cache, n_pages, block_table, bt_stride,
+                                           seq_lens, B, H_I, page_size, max_seq_len, scores, ld);
+  if (st != DSA_OK || B == 0) return st;
+  int* status = status_ptr();
+  if (!status) return DSA_ERR_CUDA;
+  IndexerArgs a{};
+  a.q_scale = q_scale; a.w = w; a.k_scale = k_scale_cache;
+  a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens; a.n_pages = n_pages;
+  a.scores = scores; a.ld = ld; a.rows = B; a.S = max_seq_len; a.page_size = page_size;
+  a.status = status; a.limit_ns = kWaitLimitNs;
+  return from_cuda(launch_indexer(q8, k8_cache, n_pages * page_size, H_I, true, max_seq_len, a, stream));
+}
+
+dsa_status_t dsa_topk(const float* scores, int64_t ld, int T, const int32_t* row_lens, int64_t n_cols,
+                      int64_t q_pos0, int k, int32_t* idx, dsa_stream_t stream) {
+  dsa_status_t st = check_topk_args(scores, ld, T, n_cols, q_pos0, k, idx, row_lens);
+  if (st != DSA_OK || T == 0) return st;
+  TopkArgs a{scores, ld, T, row_lens, n_cols, q_pos0, k, idx};
+  return from_cuda(launch_topk(a, stream));
+}
+
+dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* block_table,
+                             int64_t bt_stride, int page_size, const int32_t* idx, int T, int H, int k,
+                             float scale, uint16_t* out, float* lse, dsa_stream_t stream) {
+  dsa_status_t st = check_attn_args(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, out);
+  if (st != DSA_OK || T == 0) return st;
+  int* status = status_ptr();
+  if (!status) return DSA_ERR_CUDA;
+  AttnArgs a{};
+  a.q = q; a.kv = kv; a.n_kv_rows = n_kv_rows; a.block_table = block_table; a.bt_stride = bt_stride;
+  a.page_size = page_size; a.idx = idx; a.T = T; a.H = H; a.k = k;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = out; a.lse = lse; a.status = status; a.limit_ns = kWaitLimitNs;
+  return from_cuda(launch_sparse_attn(a, stream));
+}
+
+size_t dsa_forward_workspace_size(const dsa_forward_args* args) {
+  FwdPlan p;
+  if (plan_forward(args, &p) != DSA_OK) return 0;
+  return p.total;
+}
+
+dsa_status_t dsa_forward(const dsa_forward_args* a, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  FwdPlan p;
+  dsa_status_t st = plan_forward(a, &p);
+  if (st != DSA_OK) return st;
+  if (!a->q8 || !a->q_scale || !a->w || !a->k8 || !a->k_scale || !a->q || !a->kv || !a->out)
+    return DSA_ERR_INVALID_ARG;
+  if (p.rows == 0) return DSA_OK;
+  if (!ws || ws_bytes < p.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
+  float* scores = static_cast<float*>(ws);
+  int32_t* idx = a->idx ? a->idx : reinterpret_cast<int32_t*>(static_cast<char*>(ws) + p.scores_bytes);
+  cudaStream_t s = stream;
+
+  if (a->mode == DSA_MODE_PREFILL) {
+    st = check_index_args(a->q8, a->q_scale, a->w, a->k8, a->k_scale, a->T, a->S, a->H_I, a->q_pos0, scores, p.ld);
+    if (st != DSA_OK) return st;
+    st = check_attn_args(a->q, a->kv, a->S, nullptr, 0, 0, idx, a->T, a->H, a->k, a->out);
+    if (st != DSA_OK) return st;
+    for (int r0 = 0; r0 < a->T; r0 += p.chunk) {
+      const int rows = std::min(p.chunk, a->T - r0);
+      const int64_t pos0 = a->q_pos0 + r0;
+      st = dsa_index(a->q8 + static_cast<int64_t>(r0) * a->H_I * 128, a->q_scale + static_cast<int64_t>(r0) * a->H_I,
+                     a->w + static_cast<int64_t>(r0) * a->H_I, a->k8, a->k_scale, rows, a->S, a->H_I, pos0, scores,
+                     p.ld, s);
+      if (st != DSA_OK) return st;
+      st = dsa_topk(scores, p.ld, rows, nullptr, a->S, pos0, a->k, idx + static_cast<int64_t>(r0) * a->k, s);
+      if (st != DSA_OK) return st;
+    }
+    return dsa_sparse_attn(a->q, a->kv, a->S, nullptr, 0, 0, idx, a->T, a->H, a->k, a->scale, a->out, a->lse, s);
+  }
+  // decode
+  st = check_paged_index_args(a->q8, a->q_scale, a->w, a->k8, a->k_scale, a->n_pages, a->block_table, a->bt_stride,
+                              a->seq_lens, a->B, a->H_I, a->page_size, a->max_seq_len, scores, p.ld);
+  if (st != DSA_OK) return st;
+  st = dsa_index_paged(a->q8, a->q_scale, a->w, a->k8, a->k_scale, a->n_pages, a->block_table, a->bt_stride,
+                       a->seq_lens, a->B, a->H_I, a->page_size, a->max_seq_len, scores, p.ld, s);
+  if (st != DSA_OK) return st;
+  st = dsa_topk(scores, p.ld, a->B, a->seq_lens, p.ld, 0, a->k, idx, s);
+  if (st != DSA_OK) return st;
+  return dsa_sparse_attn(a->q, a->kv, a->n_pages * a->page_size, a->block_table, a->bt_stride, a->page_size, idx,
+                         a->B, a->H, a->k, a->scale, a->out, a->lse, s);
+}
+
+dsa_status_t dsa_device_status(dsa_stream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
+  int* p = status_ptr();
+  if (!p) return DSA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return DSA_ERR_CUDA;
+  return static_cast<dsa_status_t>(v);
+}
+
+dsa_status_t dsa_selftest_wait_timeout(int timeout_us, dsa_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 10000000) return DSA_ERR_INVALID_ARG;
+  int* p = status_ptr();
+  if (!p) return DSA_ERR_CUDA;
+  return from_cuda(launch_wait_timeout_selftest(p, static_cast<uint64_t>(timeout_us) * 1000ull, stream));
+}
+
+}  // extern "C"

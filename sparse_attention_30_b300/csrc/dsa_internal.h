@@ -1,0 +1,78 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// Bounded waits give up after this long (about one second).
+constexpr uint64_t kWaitLimitNs = 1ull << 30;
+
+// ---------------------------------------------------------------- indexer
+
+struct IndexerArgs {
+  const float* q_scale;       // [rows, H_I]
+  const float* w;             // [rows, H_I]
+  const float* k_scale;       // prefill [S]; paged [n_pages * page_size]
+  const int32_t* block_table; // paged only
+  int64_t bt_stride;
+  const int32_t* seq_lens;    // paged only
+  int64_t n_pages;
+  float* scores;
+  int64_t ld;
+  int rows;                   // prefill: T query rows; paged: B sequences
+  int S;                      // prefill: number of keys; paged: max_seq_len
+  int64_t q_pos0;
+  int page_size;
+  int tiles_per_cta;          // 128-key tiles handled by one CTA
+  int* status;
+  uint64_t limit_ns;
+};
+
+// q8 viewed as [rows * H_I, 128] bytes, k8 as [n_keys, 128] bytes (paged: n_pages * page_size).
+cudaError_t launch_indexer(const uint8_t* q8, const uint8_t* k8, int64_t n_key_rows, int H_I, bool paged,
+                           int max_keys, const IndexerArgs& a, cudaStream_t stream);
+int indexer_supported_heads(int H_I, bool paged);
+
+// ---------------------------------------------------------------- top-k
+
+struct TopkArgs {
+  const float* scores;
+  int64_t ld;
+  int T;
+  const int32_t* row_lens;
+  int64_t n_cols;
+  int64_t q_pos0;
+  int k;
+  int32_t* idx;
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- sparse attention
+
+struct AttnArgs {
+  const uint16_t* q;          // [T, H, 576] bf16
+  const uint16_t* kv;         // [n_kv_rows, 576] bf16
+  int64_t n_kv_rows;
+  const int32_t* block_table; // NULL: contiguous
+  int64_t bt_stride;
+  int page_size;
+  const int32_t* idx;         // [T, k]
+  int T, H, k;
+  float scale_log2;           // softmax scale * log2(e)
+  uint16_t* out;              // [T, H, 512] bf16
+  float* lse;                 // [T, H] or NULL
+  int* status;
+  uint64_t limit_ns;
+};
+cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- self test
+
+cudaError_t launch_wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace dsa

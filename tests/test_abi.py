@@ -1,0 +1,155 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function include/dsa.h
+declares, rejects bad arguments on the host before touching CUDA, and the Python mirror
+of dsa_forward_args has the C layout."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+def _lib():
+    from sparse_attention_30_b300 import build
+    build.build()
+    import sparse_attention_30_b300 as dsa
+    return dsa
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("dsa_index", "dsa_index_paged", "dsa_topk", "dsa_sparse_attn", "dsa_forward",
+              "dsa_forward_workspace_size", "dsa_device_status", "dsa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    dsa = _lib()
+    out = subprocess.run(["nm", "-D", "--defined-only", dsa.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\bT (dsa_[a-z_]+)\b", out.stdout))
+    for n in _declared_functions():
+        assert n in exported, n
+        assert hasattr(dsa.lib, n)
+    assert set(dsa.EXPORTS) == set(_declared_functions())
+
+
+def test_status_strings_and_version():
+    dsa = _lib()
+    for code, name in dsa.STATUS_NAMES.items():
+        assert dsa.lib.dsa_status_string(code).decode() == name
+    assert dsa.lib.dsa_status_string(99).decode() == "DSA_ERR_UNKNOWN"
+    assert dsa.lib.dsa_version() >> 16 == 1
+
+
+# Fake, 16-byte-aligned "device" addresses: validation must reject the call before any of
+# them is dereferenced or any CUDA call is made.
+A = 1 << 20
+
+
+def test_index_rejects_bad_arguments_on_host():
+    dsa = _lib()
+    f = dsa.lib.dsa_index
+    ok = dict(q8=A, qs=A, w=A, k8=A, ks=A, T=4, S=8, H=64, pos=0, sc=A, ld=8)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["q8"], a["qs"], a["w"], a["k8"], a["ks"], a["T"], a["S"], a["H"], a["pos"], a["sc"], a["ld"], None)
+
+    assert call(q8=None) == 1
+    assert call(k8=A + 8) == 1          # misaligned
+    assert call(ld=6) == 1              # ld % 4
+    assert call(ld=4, T=8) == 1         # ld < min(S, pos + T)
+    assert call(ld=4) == 4              # valid: with no GPU here it fails at the CUDA call
+    assert call(H=48) == 1              # not a power of two
+    assert call(H=256) == 1
+    assert call(S=0) == 1
+    assert call(pos=-1) == 1
+    assert call(T=0) == 0               # empty is a no-op with nothing launched
+
+
+def test_paged_index_rejects_unsupported_heads_and_pages():
+    dsa = _lib()
+    f = dsa.lib.dsa_index_paged
+
+    def call(H=64, page=64, bt_stride=2, max_len=128, ld=128, B=1):
+        return f(A, A, A, A, A, 4, A, bt_stride, A, B, H, page, max_len, A, ld, None)
+
+    assert call(H=16) == 2              # decode tiles need H_I >= 64
+    assert call(page=48) == 1
+    assert call(page=256) == 1
+    assert call(bt_stride=1) == 1       # fewer table entries than max_len needs
+    assert call(ld=64) == 1
+    assert call(B=0) == 0
+
+
+def test_topk_and_attention_reject_bad_arguments_on_host():
+    dsa = _lib()
+    t = dsa.lib.dsa_topk
+    assert t(A, 8, 2, None, 8, 0, 0, A, None) == 1        # k = 0
+    assert t(A, 8, 2, None, 16, 0, 4, A, None) == 1       # n_cols > ld
+    assert t(A, 6, 2, None, 6, 0, 4, A, None) == 1        # ld % 4
+    assert t(None, 8, 2, None, 8, 0, 4, A, None) == 1
+    assert t(A, 8, 0, None, 8, 0, 4, A, None) == 0
+    s = dsa.lib.dsa_sparse_attn
+    assert s(A, A, 10, None, 0, 0, A, 2, 129, 4, 0.1, A, None, None) == 2   # H > 128
+    assert s(A, A + 2, 10, None, 0, 0, A, 2, 8, 4, 0.1, A, None, None) == 1
+    assert s(A, A, 0, None, 0, 0, A, 2, 8, 4, 0.1, A, None, None) == 1
+    assert s(A, A, 10, None, 0, 0, A, 0, 8, 4, 0.1, A, None, None) == 0
+
+
+def test_forward_workspace_and_validation():
+    dsa = _lib()
+    a = dsa.ForwardArgs(mode=dsa.MODE_PREFILL, H_I=64, H=128, k=2048, scale=0.07, T=4096, S=4096, q_pos0=0,
+                        chunk_rows=1024)
+    n = dsa.lib.dsa_forward_workspace_size(ctypes.byref(a))
+    # one 1024-row fp32 score block plus the int32 selection of all rows
+    assert n == 1024 * 4096 * 4 + 4096 * 2048 * 4
+    a.T = 5000                                        # q_pos0 + T > S
+    assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(a)) == 0
+    d = dsa.ForwardArgs(mode=dsa.MODE_DECODE, H_I=64, H=128, k=2048, scale=0.07, B=64, page_size=64,
+                        n_pages=32768, bt_stride=512, max_seq_len=32768)
+    assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(d)) == 64 * 32768 * 4 + 64 * 2048 * 4
+    d.mode = 7
+    assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(d)) == 0
+    d.mode = dsa.MODE_DECODE
+    # null inputs are rejected before the workspace is even looked at
+    assert dsa.lib.dsa_forward(ctypes.byref(d), None, 0, None) == 1
+
+
+def test_forward_args_layout_matches_c():
+    dsa = _lib()
+    fields = [f for f, _ in dsa.ForwardArgs._fields_]
+    src = "#include <stdio.h>\n#include <stddef.h>\n#include \"dsa.h\"\nint main(void){\n"
+    src += 'printf("%zu\\n", sizeof(dsa_forward_args));\n'
+    for f in fields:
+        src += f'printf("%zu\\n", offsetof(dsa_forward_args, {f}));\n'
+    src += "return 0;}\n"
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        vals = [int(x) for x in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(dsa.ForwardArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(dsa.ForwardArgs, f).offset == off, f
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "sparse_attention_30_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), fn
+                assert "oracle/" not in text, fn

@@ -1,0 +1,303 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Criteria (written here, applied per row):
+  * indexer scores: |gpu - oracle| <= 3e-5 * sum_j |w'_j| |logit_j| + 1e-30, i.e. fp32 rounding of
+    the 64-term head sum (each term's logit is exact from the FP8 tensor-core product);
+  * top-k: index sets equal, except positions whose oracle score lies within 1e-4 (relative)
+    of the oracle's k-th score (genuine near-ties); sizes, distinctness, range and
+    causality always exact;
+  * attention: against the oracle run on the GPU's own index set, max |err| <= 2e-2 and
+    mean |err| <= 2e-3 (bf16 output); lse within 2e-3 absolute.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+MAX_TOL, MEAN_TOL, LSE_TOL, SCORE_REL = 2e-2, 2e-3, 2e-3, 3e-5
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_attention_30_b300 import build
+    build.build()
+    import sparse_attention_30_b300 as m
+    return m
+
+
+def _cuda(inp):
+    return {k: v.cuda() for k, v in inp.items()}
+
+
+def _host(inp):
+    return {k: v.cpu() for k, v in inp.items()}
+
+
+def _score_mass(q8_t, sq_t, w_t, k8, sk, n):
+    q = oracle.e4m3_to_f64(q8_t.numpy())
+    k = oracle.e4m3_to_f64(k8[:n].numpy())
+    logits = (q @ k.T) * sq_t.double().numpy()[:, None] * sk[:n].double().numpy()[None, :]
+    return np.abs(w_t.double().numpy()) @ np.abs(logits)
+
+
+def _check_scores(gpu_row, ref, mass, where):
+    err = np.abs(gpu_row.astype(np.float64) - ref)
+    bad = err > SCORE_REL * mass + 1e-30
+    assert not bad.any(), f"{where}: {bad.sum()} scores off, worst {err.max():.3g} (mass {mass[bad][:3]})"
+
+
+def _check_attention(o_gpu, lse_gpu, o_ref, lse_ref, where):
+    mx, mean = oracle.attention_error(o_ref, o_gpu)
+    assert mx <= MAX_TOL and mean <= MEAN_TOL, f"{where}: attention max {mx:.3g} mean {mean:.3g}"
+    if lse_gpu is not None:
+        d = np.abs(lse_gpu - lse_ref).max()
+        assert d <= LSE_TOL, f"{where}: lse err {d:.3g}"
+
+
+def _check_row(hinp, t, k, scale, idx_row, o_row, lse_row, q_pos0=0, decode=False, where=""):
+    r = oracle.decode_row(hinp, t, k, scale) if decode else oracle.prefill_row(hinp, t, k, scale, q_pos0)
+    ok, nswap, msg = oracle.index_sets_match(r["scores"], r["idx"], idx_row)
+    assert ok, f"{where} row {t}: {msg}"
+    use = idx_row[idx_row >= 0]
+    if decode:
+        n = int(hinp["seq_lens"][t])
+        kv = oracle.decode_gather(hinp["kv_cache"], hinp["block_table"][t], n, hinp["kv_cache"].shape[1])
+    else:
+        kv = hinp["kv"]
+        assert use.max() <= q_pos0 + t
+    o_ref, lse_ref = oracle.attention_row(hinp["q"][t], kv[torch.as_tensor(use)], scale)
+    _check_attention(o_row, lse_row, o_ref, lse_ref, f"{where} row {t}")
+    return nswap
+
+
+# ----------------------------------------------------------------------------- indexer
+
+
+@pytest.mark.parametrize("cid,rows,q_pos0", [(1, None, 0), (2, (1000, 1777), 1000), (2, (0, 4096), 0)])
+def test_indexer_matches_oracle(dsa, cid, rows, q_pos0):
+    cfg = synth.config(cid)
+    hinp = synth.prefill_inputs(cfg)
+    r0, r1 = rows if rows else (0, cfg.L)
+    d = _cuda(hinp)
+    sl = slice(r0, r1)
+    sc = dsa.index(d["q8"][sl].contiguous(), d["q_scale"][sl].contiguous(), d["w"][sl].contiguous(), d["k8"],
+                   d["k_scale"], q_pos0=q_pos0)
+    torch.cuda.synchronize()
+    assert dsa.device_status() == 0
+    sc = sc.cpu().numpy()
+    T = r1 - r0
+    check = range(T) if T <= 256 else sorted(set([0, 1, 2, 3, T - 1, T - 2] + list(range(0, T, 97))))
+    for i in check:
+        t = r0 + i
+        n = min(cfg.L, q_pos0 + i + 1)
+        ref = oracle.indexer_row(hinp["q8"][t], hinp["q_scale"][t], hinp["w"][t], hinp["k8"], hinp["k_scale"], n)
+        mass = _score_mass(hinp["q8"][t], hinp["q_scale"][t], hinp["w"][t], hinp["k8"], hinp["k_scale"], n)
+        _check_scores(sc[i, :n], ref, mass, f"cfg{cid} row {t}")
+
+
+def test_indexer_paged_matches_oracle(dsa):
+    cfg = synth.config(3, B=6, ctx=5000)
+    hinp = synth.decode_inputs(cfg)
+    d = _cuda(hinp)
+    sc = dsa.index_paged(d["q8"], d["q_scale"], d["w"], d["k8_cache"], d["k_scale_cache"], d["block_table"],
+                         d["seq_lens"], 5000)
+    assert dsa.device_status() == 0
+    sc = sc.cpu().numpy()
+    page = cfg.page
+    for b in range(cfg.B):
+        n = int(hinp["seq_lens"][b])
+        k8 = oracle.decode_gather(hinp["k8_cache"], hinp["block_table"][b], n, page)
+        ks = oracle.decode_gather(hinp["k_scale_cache"], hinp["block_table"][b], n, page)
+        ref = oracle.indexer_row(hinp["q8"][b], hinp["q_scale"][b], hinp["w"][b], k8, ks, n)
+        mass = _score_mass(hinp["q8"][b], hinp["q_scale"][b], hinp["w"][b], torch.as_tensor(k8),
+                           torch.as_tensor(ks), n)
+        _check_scores(sc[b, :n], ref, mass, f"paged seq {b}")
+
+
+# ----------------------------------------------------------------------------- top-k
+
+
+def _topk_valid(vals, sel, k):
+    n = len(vals)
+    m = min(k, n)
+    sel = sel[sel >= 0]
+    assert len(sel) == m and len(np.unique(sel)) == m and sel.min() >= 0 and sel.max() < n
+    if m == n:
+        return
+    kth = np.sort(vals)[::-1][m - 1]
+    assert np.all(vals[sel] >= kth)
+    strict = np.nonzero(vals > kth)[0]
+    assert np.isin(strict, sel).all()
+
+
+@pytest.mark.parametrize("dist", ["normal", "ties", "const", "lognormal", "negative", "tiny_range"])
+@pytest.mark.parametrize("n,k", [(100, 64), (2049, 2048), (4097, 2048), (131072, 2048), (70000, 64), (3000, 1)])
+def test_topk_exact_on_fixed_scores(dsa, dist, n, k):
+    rng = np.random.default_rng(n * 7 + k)
+    T = 3
+    if dist == "normal":
+        v = rng.standard_normal((T, n))
+    elif dist == "ties":
+        v = rng.integers(0, 4, (T, n)).astype(np.float64)
+    elif dist == "const":
+        v = np.full((T, n), 0.5)
+    elif dist == "lognormal":
+        v = rng.lognormal(0, 2.0, (T, n))
+    elif dist == "negative":
+        v = -np.abs(rng.standard_normal((T, n))) * 1e3
+    else:
+        v = 1.0 + rng.integers(0, 50, (T, n)) * 2.0 ** -23
+    v = v.astype(np.float32)
+    ld = (n + 3) // 4 * 4
+    sc = torch.full((T, ld), float("nan"), dtype=torch.float32)
+    sc[:, :n] = torch.from_numpy(v)
+    lens = torch.tensor([n, max(1, n // 3), n], dtype=torch.int32)
+    idx = dsa.topk(sc.cuda(), k, row_lens=lens.cuda())
+    assert dsa.device_status() == 0
+    idx = idx.cpu().numpy()
+    for r in range(T):
+        nr = int(lens[r])
+        _topk_valid(v[r, :nr].astype(np.float64), idx[r], k)
+        assert np.all(idx[r, min(k, nr):] == -1)
+
+
+def test_topk_causal_prefix_rows(dsa):
+    rng = np.random.default_rng(3)
+    T, S, k, q_pos0 = 300, 5000, 2048, 1900
+    v = rng.standard_normal((T, S)).astype(np.float32)
+    idx = dsa.topk(torch.from_numpy(v).cuda(), k, q_pos0=q_pos0, n_cols=S).cpu().numpy()
+    for t in range(T):
+        n = min(S, q_pos0 + t + 1)
+        _topk_valid(v[t, :n].astype(np.float64), idx[t], k)
+
+
+# ----------------------------------------------------------------------------- attention
+
+
+def test_attention_with_oracle_selection_config1(dsa):
+    cfg = synth.config(1)
+    hinp = synth.prefill_inputs(cfg)
+    rows = oracle.prefill_rows(hinp, range(cfg.L), cfg.k, cfg.scale)
+    idx = torch.tensor(np.stack([np.pad(r["idx"], (0, cfg.k - len(r["idx"])), constant_values=-1)
+                                 for r in rows]), dtype=torch.int32)
+    d = _cuda(hinp)
+    out, lse = dsa.sparse_attn(d["q"], d["kv"], idx.cuda(), cfg.scale)
+    assert dsa.device_status() == 0
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    for t, r in enumerate(rows):
+        _check_attention(out[t], lse[t], r["o"], r["lse"], f"cfg1 row {t}")
+
+
+def test_attention_ragged_selection_and_range_errors(dsa):
+    g = torch.Generator().manual_seed(11)
+    T, H, S, k = 5, 128, 3000, 100
+    q = torch.randn(T, H, 576, generator=g).to(torch.bfloat16)
+    kv = torch.randn(S, 576, generator=g).to(torch.bfloat16)
+    idx = torch.full((T, k), -1, dtype=torch.int32)
+    counts = [100, 1, 33, 64, 0]
+    for t, c in enumerate(counts):
+        idx[t, :c] = torch.randperm(S, generator=g)[:c].to(torch.int32)
+    out, lse = dsa.sparse_attn(q.cuda(), kv.cuda(), idx.cuda(), 0.07)
+    assert dsa.device_status() == 0
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    for t, c in enumerate(counts):
+        o_ref, l_ref = oracle.attention_row(q[t], kv[idx[t, :c].long()], 0.07)
+        if c == 0:
+            assert np.all(out[t] == 0) and np.all(np.isneginf(lse[t]))
+        else:
+            _check_attention(out[t], lse[t], o_ref, l_ref, f"row {t}")
+    # an index past the end is skipped and reported
+    bad = idx.clone()
+    bad[0, 5] = S + 7
+    out2, _ = dsa.sparse_attn(q.cuda(), kv.cuda(), bad.cuda(), 0.07)
+    assert dsa.device_status() == 6
+    keep = torch.cat([idx[0, :5], idx[0, 6:100]]).long()
+    o_ref, _ = oracle.attention_row(q[0], kv[keep], 0.07)
+    _check_attention(out2.float().cpu().numpy()[0], None, o_ref, None, "range row")
+
+
+# ----------------------------------------------------------------------------- fused forward
+
+
+def _run_prefill(dsa, d, cfg, chunk_rows=0):
+    idx = torch.empty((cfg.L, cfg.k), dtype=torch.int32, device="cuda")
+    lse = torch.empty((cfg.L, cfg.H), dtype=torch.float32, device="cuda")
+    f = dsa.Forward.prefill(d, cfg.k, cfg.scale, chunk_rows=chunk_rows, lse=lse, idx=idx)
+    f()
+    assert dsa.device_status() == 0
+    return f
+
+
+def test_forward_prefill_config1_all_rows(dsa):
+    cfg = synth.config(1)
+    hinp = synth.prefill_inputs(cfg)
+    f = _run_prefill(dsa, _cuda(hinp), cfg, chunk_rows=100)
+    idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
+    for t in range(cfg.L):
+        _check_row(hinp, t, cfg.k, cfg.scale, idx[t], out[t], lse[t], where="cfg1")
+
+
+def test_forward_prefill_config2_sampled_rows(dsa):
+    cfg = synth.config(2)
+    hinp = synth.prefill_inputs(cfg)
+    f = _run_prefill(dsa, _cuda(hinp), cfg, chunk_rows=1000)
+    idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
+    rows = sorted(set([0, 1, 2, 3, 999, 1000, 2046, 2047, 2048, 2049, 4094, 4095] + list(range(5, 4096, 61))))
+    swaps = sum(_check_row(hinp, t, cfg.k, cfg.scale, idx[t], out[t], lse[t], where="cfg2") for t in rows)
+    assert swaps <= len(rows)  # near-tie swaps are rare
+
+
+@pytest.mark.parametrize("cid", [3, 5])
+def test_forward_decode_full_config(dsa, cid):
+    cfg = synth.config(cid)
+    d = synth.decode_inputs(cfg, device="cuda")
+    max_len = int(d["seq_lens"].max())
+    idx = torch.empty((cfg.B, cfg.k), dtype=torch.int32, device="cuda")
+    lse = torch.empty((cfg.B, cfg.H), dtype=torch.float32, device="cuda")
+    f = dsa.Forward.decode(d, cfg.k, cfg.scale, max_len, lse=lse, idx=idx)
+    f()
+    assert dsa.device_status() == 0
+    hinp = _host(d)
+    idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
+    for b in range(cfg.B):
+        _check_row(hinp, b, cfg.k, cfg.scale, idx[b], out[b], lse[b], decode=True, where=f"cfg{cid}")
+
+
+def test_forward_prefill_config4_full_size_sampled_rows(dsa):
+    """128K prefill at full size, launched exactly as the bench launches it; sampled rows."""
+    cfg = synth.config(4)
+    d = synth.prefill_inputs(cfg, device="cuda")
+    f = dsa.Forward.prefill(d, cfg.k, cfg.scale, lse=torch.empty((cfg.L, cfg.H), device="cuda"),
+                            idx=torch.empty((cfg.L, cfg.k), dtype=torch.int32, device="cuda"))
+    f()
+    assert dsa.device_status() == 0
+    rows = [0, 1, 2047, 2048, 5000, 65535, 65536, 100003, 131070, 131071]
+    keys = {n: d[n].cpu() for n in ("k8", "k_scale", "kv")}
+    for t in rows:
+        # only the sampled query rows are copied to the host; the oracle reads them by row number
+        row_inp = dict(keys, **{n: {t: d[n][t].cpu()} for n in ("q8", "q_scale", "w", "q")})
+        r = oracle.prefill_row(row_inp, t, cfg.k, cfg.scale)
+        idx_t = f.idx[t].cpu().numpy()
+        ok, _, msg = oracle.index_sets_match(r["scores"], r["idx"], idx_t)
+        assert ok, f"cfg4 row {t}: {msg}"
+        use = idx_t[idx_t >= 0]
+        o_ref, lse_ref = oracle.attention_row(row_inp["q"][t], keys["kv"][torch.as_tensor(use)], cfg.scale)
+        _check_attention(f.out[t].float().cpu().numpy(), f.lse[t].cpu().numpy(), o_ref, lse_ref, f"cfg4 row {t}")
+
+
+# ----------------------------------------------------------------------------- failure path
+
+
+def test_bounded_wait_times_out_and_context_survives(dsa):
+    assert dsa.device_status() == 0
+    assert dsa.selftest_wait_timeout(2000) == 5     # DSA_ERR_DEVICE_TIMEOUT, recorded and returned
+    assert dsa.device_status() == 0                 # cleared
+    x = torch.randn(2, 4096, device="cuda")
+    idx = dsa.topk(x, 16)
+    assert dsa.device_status() == 0 and idx.shape == (2, 16)
