@@ -200,9 +200,10 @@ def run_ours(args, dist, rank, ws):
     import sparse_attention_30_b300 as dsa
 
     peaks = _peaks()
-    cfg = synth.config(4)
+    cid = {"prefill128k": 4, "prefill4k": 2}[args.workload]
+    cfg = synth.config(cid)
     if rank:
-        cfg = synth.config(4, seed=cfg.seed + 1000 * rank)
+        cfg = synth.config(cid, seed=cfg.seed + 1000 * rank)
     d = synth.prefill_inputs(cfg, device="cuda")
     runner = PrefillRunner(dsa, d, cfg, args.chunk)
 
@@ -257,9 +258,10 @@ def run_ours(args, dist, rank, ws):
             "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 indexer / bf16 attention (fp32 accum)",
             "data": "synthetic (seeded; shapes and distributions of the 128K prefill workload)",
-            "config": {"workload": "prefill L=131072 (128K), H_I=64, d_I=128, k=2048, H=128, D=576/512",
+            "config": {"workload": f"prefill L={cfg.L}, H_I=64, d_I=128, k=2048, H=128, D=576/512",
                        "seq_len": cfg.L, "global_batch": ws, "chunk_rows": args.chunk,
-                       "l2": "inputs larger than L2 (Q 19.3 GB, O 17.2 GB per step)", "parallelism": f"dp{ws}"},
+                       "l2": "inputs larger than L2 (Q %.1f GB, O %.1f GB per step)"
+                             % (cfg.L * cfg.H * 1152 / 1e9, cfg.L * cfg.H * 1024 / 1e9), "parallelism": f"dp{ws}"},
             "roofline": roofline,
             "kernels": {n: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         for n, v in kern.items()},
@@ -432,6 +434,8 @@ def main():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--chunk", type=int, default=8192)
+    p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k"],
+                   help="prefill4k is the small case used for profiler captures")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
