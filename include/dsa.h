@@ -222,6 +222,29 @@ dsa_status_t dsa_device_status(dsa_stream_t stream);
  */
 dsa_status_t dsa_selftest_wait_timeout(int timeout_us, dsa_stream_t stream);
 
+/*
+ * dsa_decode_noalloc — the decode forward (mode DSA_MODE_DECODE of dsa_forward) for callers
+ * that cannot allocate device memory.  The paper has no counterpart: this is a deployment
+ * convenience.  Some callers may not call cudaMalloc themselves (a plugin inside a serving
+ * engine that owns all device memory, a decode loop that cannot afford an allocation's
+ * implicit synchronisation); instead of a caller-supplied workspace this call takes its
+ * scratch (fp32 scores and, if args->idx is NULL, the selection) from a fixed array of
+ * dsa_decode_noalloc_capacity() bytes (20 MiB) that the library keeps in the device memory
+ * of every GPU that loads it, until the process exits.
+ *   - Needs B * round4(max_seq_len) * 4 + B * k * 4 bytes (each rounded up to 256); a
+ *     larger request returns DSA_ERR_WORKSPACE without launching anything.
+ *   - The first call on a device (with that device current) looks up the array's address;
+ *     make that first call before any stream capture.
+ *   - Every call shares the array: calls whose work overlaps on the GPU race on it and
+ *     must be ordered by the caller.  Nothing in it needs clearing between calls.
+ *   - Otherwise identical to dsa_forward in decode mode (same kernels, same outputs);
+ *     it allocates nothing and calls no allocating routine.
+ */
+dsa_status_t dsa_decode_noalloc(const dsa_forward_args* args, dsa_stream_t stream);
+
+/* Size in bytes of the fixed scratch array dsa_decode_noalloc uses. */
+size_t dsa_decode_noalloc_capacity(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -2,8 +2,8 @@
 
 Argument marshalling only: every step of the computation runs in the CUDA kernels of
 libdsa.so (see include/dsa.h for the exact contract of each call).  PyTorch supplies
-device memory and the current stream.  Importing this module loads the library and
-raises if it has not been built (python -m sparse_attention_30_b300.build).
+device memory and the current stream.  Importing this module (re)builds libdsa.so if a
+source is newer than it, loads it, and raises if either step fails.
 """
 from __future__ import annotations
 
@@ -22,7 +22,8 @@ MODE_PREFILL, MODE_DECODE = 0, 1
 
 # Names of every function include/dsa.h declares.
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_index", "dsa_index_paged", "dsa_topk", "dsa_sparse_attn",
-           "dsa_forward_workspace_size", "dsa_forward", "dsa_device_status", "dsa_selftest_wait_timeout")
+           "dsa_forward_workspace_size", "dsa_forward", "dsa_device_status", "dsa_selftest_wait_timeout",
+           "dsa_decode_noalloc", "dsa_decode_noalloc_capacity")
 
 
 class DSAError(RuntimeError):
@@ -47,8 +48,13 @@ class ForwardArgs(ctypes.Structure):
 
 
 def _load():
+    from . import build as _build
+    try:
+        _build.build()  # compiles only when a source is newer than the library
+    except Exception as e:  # no silent fallback: the package is unusable without its kernels
+        raise ImportError(f"libdsa.so could not be built: {e}") from e
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libdsa.so is not built ({LIB_PATH}); run python -m sparse_attention_30_b300.build")
+        raise ImportError(f"libdsa.so is missing ({LIB_PATH})")
     lib = ctypes.CDLL(LIB_PATH)
     P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
     sig = {
@@ -62,6 +68,8 @@ def _load():
         "dsa_forward": ([ctypes.POINTER(ForwardArgs), P, ctypes.c_size_t, P], I),
         "dsa_device_status": ([P], I),
         "dsa_selftest_wait_timeout": ([I, P], I),
+        "dsa_decode_noalloc": ([ctypes.POINTER(ForwardArgs), P], I),
+        "dsa_decode_noalloc_capacity": ([], ctypes.c_size_t),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
