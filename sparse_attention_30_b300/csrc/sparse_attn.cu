@@ -4,19 +4,21 @@
 // Every head of token t sees the same rows c_s, so per token this is a dense
 // [H x 576] x [576 x |S_t|] product followed by [H x |S_t|] x [|S_t| x 512].
 //
-// Layout on the chip (one CTA = one token x one half of the value dims):
-//   TMEM (512 columns): O half [128 heads x 256] fp32 at columns 0..255,
-//                       S tile [128 heads x 32 keys] fp32 at columns 256..287.
-//   SMEM: Q [128 x 576] bf16 as 9 K-major 128B-swizzled blocks of 64 dims;
-//         two buffers of 32 gathered latent rows in the same layout (the QK^T B operand,
-//         and, read MN-major, the PV B operand); P [128 x 32] bf16, 64B-swizzled.
-// The output does not fit TMEM for all 512 value dims next to S, so the two value halves
-// run in two CTAs that both compute S (QK^T is recomputed once per half).
+// One token runs on a cluster of two CTAs with different jobs, and data flows one way:
 //
-// Per 32-key tile: cp.async gather of the next tile overlaps the current tile's
-// S = Q K^T (tcgen05.mma, 36 x K16), the softmax (thread = head = TMEM lane),
-// and O += P V (2 x K16, N = 256).  The running max is only moved when it grows by more
-// than 2^8 (log2 domain), which rescales O in TMEM; the final 1/l is applied on the way out.
+//   rank 0, "score" CTA: Q [128 x 576] bf16 sits in TMEM (A operand of the MMA read straight
+//     from tensor memory), S = Q K^T is computed 32 keys at a time into four TMEM buffers from
+//     K rows gathered by eight cp.async warps into a 5-stage shared-memory ring, and four warps
+//     (one head row per thread) run the online softmax.  Each 32-key tile of P (bf16) plus per-row rescale factors is
+//     pushed into rank 1's shared memory with an asynchronous bulk copy.
+//   rank 1, "value" CTA: O [128 x 512] fp32 fills its whole TMEM; eight warps gather the value
+//     part (first 512 latent dims) of the same rows into a 4-stage ring and it runs O += P V as soon
+//     as a P tile lands.  When rank 0 moved a row's running max (lazily: only when it grows
+//     by more than 2^8), the factor travels with P and O is rescaled before that tile's PV.
+//     Ring slots are handed back to rank 0 by a credit warp, off the critical path.
+//
+// Nothing is computed twice and nothing waits on a round trip between the CTAs; the MMA
+// work is 576 (S) vs 512 (PV) latent dims per key on the two SMs.
 #include <cuda_bf16.h>
 
 #include "dsa_internal.h"
@@ -25,23 +27,38 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kKT = 32;                       // keys per tile
-constexpr int kDL = 576, kDV = 512, kHalf = 256;
-constexpr int kBlocks = kDL / 64;             // 9 swizzle blocks of 64 bf16 (128 B)
-constexpr int kQBlockBytes = 128 * 128;       // 128 rows x 128 B
-constexpr int kQBytes = kBlocks * kQBlockBytes;
-constexpr int kKVBlockBytes = kKT * 128;
-constexpr int kKVBytes = kBlocks * kKVBlockBytes;
-constexpr int kPBytes = 128 * kKT * 2;
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kQBytes;
-constexpr int kOffP = kOffKV + 2 * kKVBytes;
-constexpr int kSmem = kOffP + kPBytes + 1024;  // + alignment slack
-constexpr int kChunksPerRow = kDL * 2 / 16;   // 72 16-byte chunks per latent row
+constexpr int kThreads = 448;                  // 14 warps
+constexpr int kProdWarps = 8;                  // warps 1-8 gather
+constexpr int kProducers = kProdWarps * 32;
+constexpr int kRowWarp0 = 1 + kProdWarps;      // warps 9-12: one head row per thread (TMEM lane)
+constexpr int kCreditWarp = kRowWarp0 + 4;     // warp 13 (rank 1): slot credits
+constexpr int kKT = 32;                        // keys per tile
+constexpr int kDL = 576, kDV = 512;
+constexpr int kKStages = 5, kVStages = 4, kSlots = 6, kSBufs = 4;
+constexpr int kLag = 2;                        // gather signals tile i - kLag after issuing tile i
+constexpr int kBlockBytes = kKT * 128;         // 32 rows x 64 bf16
+constexpr int kKStageBytes = 9 * kBlockBytes;  // 36 KB: all 576 dims
+constexpr int kVStageBytes = 8 * kBlockBytes;  // 32 KB: value dims 0..511
+// P slot: P [128 x 32] bf16 (64B-swizzled) | 128 fp32 factors | 4 int flags (one per row warp)
+constexpr int kSlotP = 128 * kKT * 2;
+constexpr int kSlotFac = kSlotP;
+constexpr int kSlotFlag = kSlotFac + 128 * 4;
+constexpr int kSlotBytes = kSlotFlag + 16;     // bytes moved per tile
+constexpr int kSlotStride = 9216;
+constexpr int kStatsBytes = 1024;              // l[128], m[128]
+// rank 0 layout
+constexpr int kOffK = 0;
+constexpr int kOffStage = kOffK + kKStages * kKStageBytes;
+constexpr int kEnd0 = kOffStage + 2 * kSlotStride;
+// rank 1 layout
+constexpr int kOffV = 0;
+constexpr int kOffSlots = kOffV + kVStages * kVStageBytes;
+constexpr int kOffStats = kOffSlots + kSlots * kSlotStride;
+constexpr int kEnd1 = kOffStats + kStatsBytes;
+constexpr int kSmem = (kEnd0 > kEnd1 ? kEnd0 : kEnd1) + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 256;
-constexpr float kRescaleThreshold = 8.0f;     // log2 units
+constexpr uint32_t kColS = 288;                // rank 0: Q in columns 0..287, S buffers after it
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -54,236 +71,422 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Physical latent row of selected position s for token t, or -1 if the slot is empty or
-// the position / page is out of range.
+// Physical latent row of position s for row t, or -1 if the slot is empty or out of range.
 __device__ __forceinline__ int64_t latent_row(const AttnArgs& a, int t, int32_t s, bool* range_err) {
   if (s < 0) return -1;
   if (a.block_table == nullptr) {
     if (s >= a.n_kv_rows) { *range_err = true; return -1; }
     return s;
   }
-  if (s / a.page_size >= a.bt_stride) { *range_err = true; return -1; }  // past this row of the table
+  if (s / a.page_size >= a.bt_stride) { *range_err = true; return -1; }
   const int32_t page = a.block_table[static_cast<int64_t>(t) * a.bt_stride + s / a.page_size];
   const int64_t r = static_cast<int64_t>(page) * a.page_size + s % a.page_size;
   if (page < 0 || r >= a.n_kv_rows) { *range_err = true; return -1; }
   return r;
 }
 
-// Gathers the 32 latent rows of tile `tile` into KV buffer `dst` (9 swizzled blocks).
-__device__ __forceinline__ void gather_tile(const AttnArgs& a, int t, int tile, uint32_t dst,
-                                            int32_t* s_valid, bool* range_err) {
-  const int32_t* idx = a.idx + static_cast<int64_t>(t) * a.k;
-  for (int q = threadIdx.x; q < kKT * kChunksPerRow; q += kThreads) {
-    const int r = q / kChunksPerRow, cc = q % kChunksPerRow;
-    const int slot = tile * kKT + r;
-    const int32_t s = slot < a.k ? __ldg(idx + slot) : -1;
-    const int64_t pr = latent_row(a, t, s, range_err);
-    const int blk = cc >> 3, c = cc & 7;
-    const uint32_t d = dst + blk * kKVBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
-    const uint16_t* src = a.kv + (pr < 0 ? 0 : pr * kDL) + cc * 8;
-    ptx::cp_async16(d, src, pr >= 0);
-    if (cc == 0) s_valid[r] = pr >= 0;
+struct Bars {
+  // rank 0
+  uint64_t k_full[kKStages], k_empty[kKStages], s_full[kSBufs], s_empty[kSBufs], q_ready, p_empty[kSlots];
+  // rank 1
+  uint64_t v_full[kVStages], v_empty[kVStages], p_full[kSlots], ready[kSlots], slot_free[kSlots], stats_full;
+  uint64_t mma_done;
+};
+
+__device__ __forceinline__ uint32_t baddr(const uint64_t& b) { return ptx::smem_addr(&b); }
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > limit_ns) break;
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a) {
+// Gather of tile i: `nblk` 64-dim blocks (from latent dim 0) of each of the 32 selected rows
+// into a 128B-swizzled stage.  Each producer warp copies whole rows (rows w, w + 8, ...): the
+// tile's 32 positions are read once (one per lane) and the row addresses are broadcast with
+// shuffles, so no load sits between consecutive copies; lanes move consecutive 16-byte chunks.
+__device__ __forceinline__ void gather_rows(const AttnArgs& a, int t, const int32_t* idx_row, int i, uint32_t dst,
+                                            int nblk, int pw, int lane, bool* range_err) {
+  const int slot = i * kKT + lane;
+  const int32_t s = slot < a.k ? __ldg(idx_row + slot) : -1;
+  const int64_t pr = latent_row(a, t, s, range_err);
+  const uint16_t* base = a.kv + (pr < 0 ? 0 : pr * kDL);
+  const int chunks = nblk * 8;
+  for (int r = pw; r < kKT; r += kProdWarps) {
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(base), r));
+    const bool ok = __shfl_sync(0xffffffffu, pr >= 0 ? 1 : 0, r) != 0;
+    const uint32_t drow = dst + r * 128;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int cc = lane + 32 * j;
+      if (cc < chunks) {
+        const int blk = cc >> 3, c = cc & 7;
+        ptx::cp_async16(drow + blk * kBlockBytes + ((c ^ (r & 7)) << 4), src + cc * 8, ok);
+      }
+    }
+  }
+}
+
+// Producer loop shared by both ranks: ring of `stages` stages, signalling with a lag of kLag.
+__device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const int32_t* idx_row, int n_tiles,
+                                              uint32_t ring, int stage_bytes, int stages, int nblk,
+                                              uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
+  const int pw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
+  bool range_err = false;
+  int issued = 0;
+  for (int i = 0; i < n_tiles; ++i) {
+    const int st = i % stages;
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(baddr(empty[st]), ((i / stages) & 1) ^ 1, abort_flag, a.status,
+                                                a.limit_ns)))
+      break;
+    gather_rows(a, t, idx_row, i, ring + st * stage_bytes, nblk, pw, lane, &range_err);
+    ptx::cp_async_commit();
+    ++issued;
+    if (i >= kLag) {
+      ptx::cp_async_wait<kLag>();
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(baddr(full[(i - kLag) % stages]));
+    }
+  }
+  if (issued >= 2) {
+    ptx::cp_async_wait<1>();
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive(baddr(full[(issued - 2) % stages]));
+  }
+  ptx::cp_async_wait<0>();
+  ptx::fence_proxy_async_smem();
+  if (issued >= 1) ptx::mbar_arrive(baddr(full[(issued - 1) % stages]));
+  if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag_s;
-  __shared__ int32_t s_valid[2][kKT];
+  __shared__ int n_tiles_s;
 
-  const int t = blockIdx.x, v = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int h = tid;  // head row = TMEM lane
+  const int rank = static_cast<int>(ptx::cluster_ctarank());
+  const int t = blockIdx.x >> 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &abort_flag_s;
-
-  const uint32_t sQ = ptx::smem_addr(smem + kOffQ);
-  const uint32_t sKV0 = ptx::smem_addr(smem + kOffKV);
-  const uint32_t sP = ptx::smem_addr(smem + kOffP);
-  uint8_t* pP = smem + kOffP;
-  const uint32_t bar_s = ptx::smem_addr(&bars[0]);
-  const uint32_t bar_o = ptx::smem_addr(&bars[1]);
+  const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.k;
+  const uint32_t sbase = ptx::smem_addr(smem);
 
   if (tid == 0) {
-    ptx::mbar_init(bar_s, 1);
-    ptx::mbar_init(bar_o, 1);
+    if (rank == 0) {
+      for (int s = 0; s < kKStages; ++s) {
+        ptx::mbar_init(baddr(bars.k_full[s]), kProducers);
+        ptx::mbar_init(baddr(bars.k_empty[s]), 1);
+      }
+      for (int b = 0; b < kSBufs; ++b) {
+        ptx::mbar_init(baddr(bars.s_full[b]), 1);
+        ptx::mbar_init(baddr(bars.s_empty[b]), 128);
+      }
+      ptx::mbar_init(baddr(bars.q_ready), 128);
+      for (int s = 0; s < kSlots; ++s) ptx::mbar_init(baddr(bars.p_empty[s]), 1);
+    } else {
+      for (int s = 0; s < kVStages; ++s) {
+        ptx::mbar_init(baddr(bars.v_full[s]), kProducers);
+        ptx::mbar_init(baddr(bars.v_empty[s]), 1);
+      }
+      for (int s = 0; s < kSlots; ++s) {
+        ptx::mbar_init(baddr(bars.p_full[s]), 1);
+        ptx::mbar_init(baddr(bars.ready[s]), 128);
+        ptx::mbar_init(baddr(bars.slot_free[s]), 1);
+      }
+      ptx::mbar_init(baddr(bars.stats_full), 1);
+    }
+    ptx::mbar_init(baddr(bars.mma_done), 1);
     abort_flag_s = 0;
+    // valid slots come first: the number of tiles follows from the first empty slot
+    int lo = 0, hi = a.k;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (idx_row[mid] >= 0) lo = mid + 1; else hi = mid;
+    }
+    n_tiles_s = (lo + kKT - 1) / kKT;
     ptx::fence_mbar_init();
+    if (rank == 1 && n_tiles_s > 0) {
+      // arm the first use of every P slot and the final statistics for rank 0's bulk copies
+      for (int s = 0; s < kSlots; ++s) ptx::mbar_arrive_expect_tx(baddr(bars.p_full[s]), kSlotBytes);
+      ptx::mbar_arrive_expect_tx(baddr(bars.stats_full), kStatsBytes);
+    }
   }
   if (warp == 0) {
     ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
   }
-
-  // number of 32-key tiles: valid slots come first, so stop at the first tile whose
-  // first slot is empty
-  const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.k;
-  const int max_tiles = (a.k + kKT - 1) / kKT;
-
-  // ---- Q (rows >= H are zero) and the first KV tile
-  {
-    const uint16_t* qrow = a.q + static_cast<int64_t>(t) * a.H * kDL;
-    for (int q = tid; q < 128 * kChunksPerRow; q += kThreads) {
-      const int r = q / kChunksPerRow, cc = q % kChunksPerRow;
-      const int blk = cc >> 3, c = cc & 7;
-      const uint32_t d = sQ + blk * kQBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
-      const bool ok = r < a.H;
-      ptx::cp_async16(d, qrow + (ok ? r * kDL + cc * 8 : 0), ok);
-    }
-  }
-  bool range_err = false;
-  int n_tiles = 0;
-  if (max_tiles > 0 && idx_row[0] >= 0) {
-    n_tiles = 1;
-    gather_tile(a, t, 0, sKV0, s_valid[0], &range_err);
-  }
-  ptx::cp_async_commit();
-
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync_all();  // both CTAs' barriers exist (and are armed) before any remote traffic
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tS = tmem + kColS;
-  const uint32_t tO = tmem;
+  const int n_tiles = n_tiles_s;
 
-  constexpr uint32_t kIdescS = ptx::instr_desc(128, kKT, 1, 1, 0, 0);
-  constexpr uint32_t kIdescPV = ptx::instr_desc(128, kHalf, 1, 1, 0, 1);
-  const uint64_t descQ = ptx::smem_desc(sQ, 16, 1024, ptx::kLayoutSw128);
-  const uint64_t descP = ptx::smem_desc(sP, 16, 512, ptx::kLayoutSw64);
-
-  float m_used = -INFINITY;  // running max (log2 domain) the exponentials are taken against
-  float l = 0.f;             // running sum of exp2(x - m_used)
-  uint32_t phase_s = 0, phase_o = 0;
-  bool ok = true;
-
-  for (int i = 0; ok && i < n_tiles; ++i) {
-    const int buf = i & 1;
-    const uint32_t sKV = sKV0 + buf * kKVBytes;
-    // prefetch tile i+1 into the other buffer (its previous contents were last read by
-    // the PV MMA of tile i-1, which completed before this iteration)
-    if (i + 1 < max_tiles && idx_row[(i + 1) * kKT] >= 0) {
-      n_tiles = i + 2;
-      gather_tile(a, t, i + 1, sKV0 + (buf ^ 1) * kKVBytes, s_valid[buf ^ 1], &range_err);
-    }
-    ptx::cp_async_commit();
-    ptx::cp_async_wait<1>();
-    ptx::fence_proxy_async_smem();
-    __syncthreads();
-
-    // ---- S = Q K^T for 32 keys
-    if (tid == 0) {
-      ptx::tc_fence_after();
-#pragma unroll 1
-      for (int kb = 0; kb < kBlocks; ++kb) {
-        const uint64_t da = descQ + ((kb * kQBlockBytes) >> 4);
-        const uint64_t db = ptx::smem_desc(sKV + kb * kKVBlockBytes, 16, 1024, ptx::kLayoutSw128);
+  if (rank == 0) {
+    // ================================================================ score CTA
+    if (warp == 0) {
+      if (lane == 0 && n_tiles > 0) {
+        constexpr uint32_t kIdescS = ptx::instr_desc(128, kKT, 1, 1, 0, 0);
+        bool ok = ptx::mbar_wait(baddr(bars.q_ready), 0, abort_flag, a.status, a.limit_ns);
+        ptx::tc_fence_after();
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          const int st = i % kKStages, sb = i % kSBufs;
+          if (!ptx::mbar_wait(baddr(bars.k_full[st]), (i / kKStages) & 1, abort_flag, a.status, a.limit_ns) ||
+              !ptx::mbar_wait(baddr(bars.s_empty[sb]), ((i / kSBufs) & 1) ^ 1, abort_flag, a.status,
+                              a.limit_ns))
+            break;
+          ptx::tc_fence_after();
+          const uint64_t db0 = ptx::smem_desc(sbase + kOffK + st * kKStageBytes, 16, 1024, ptx::kLayoutSw128);
+          const uint32_t d = tmem + kColS + sb * kKT;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // 16 dims = 32 B = +2 in the descriptor
-          ptx::mma_bf16(tS, da + 2 * ks, db + 2 * ks, kIdescS, (kb | ks) ? 1u : 0u);
+          for (int f = 0; f < 36; ++f)  // K = 576 = 36 x 16; A step = 8 TMEM columns, B step = 32 bytes
+            ptx::mma_bf16_ts(d, tmem + f * 8, db0 + (f >> 2) * (kBlockBytes >> 4) + 2 * (f & 3), kIdescS,
+                             f > 0 ? 1u : 0u);
+          ptx::mma_commit(baddr(bars.k_empty[st]));
+          ptx::mma_commit(baddr(bars.s_full[sb]));
+        }
+        ptx::mma_commit(baddr(bars.mma_done));
+        drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
       }
-      ptx::mma_commit(bar_s);
-    }
-    if (!ptx::mbar_wait(bar_s, phase_s, abort_flag, a.status, a.limit_ns)) { ok = false; break; }
-    phase_s ^= 1;
-    ptx::tc_fence_after();
-
-    // ---- softmax on this thread's head row
-    uint32_t sr[32];
-    ptx::tmem_ld32(tS + lane_base, sr);
-    ptx::tmem_wait_ld();
-    float x[kKT];
-    float mt = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kKT; ++j) {
-      x[j] = s_valid[buf][j] ? __uint_as_float(sr[j]) * a.scale_log2 : -INFINITY;
-      mt = fmaxf(mt, x[j]);
-    }
-    const float m_new = fmaxf(m_used, mt);
-    const bool need = (i == 0) || (m_new > m_used + kRescaleThreshold);
-    if (__any_sync(0xffffffffu, need)) {
-      // O and l are kept against m_used; move m_used up to m_new (O rescaled in TMEM)
-      const float f = (i == 0) ? 0.f : fast_exp2(m_used - m_new);
-      if (i > 0) {
+    } else if (warp <= kProdWarps) {
+      producer_loop(a, t, idx_row, n_tiles, sbase + kOffK, kKStageBytes, kKStages, 9, bars.k_full, bars.k_empty,
+                    abort_flag);
+    } else if (warp < kCreditWarp) {
+      // ------------------------------------------------------------ Q -> TMEM, then softmax
+      const int h = (warp & 3) * 32 + lane;
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      {
+        const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(t) * a.H + h) * kDL);
 #pragma unroll 1
-        for (int c = 0; c < kHalf / 32; ++c) {
-          uint32_t o[32];
-          ptx::tmem_ld32(tO + lane_base + c * 32, o);
-          ptx::tmem_wait_ld();
+        for (int c = 0; c < 9; ++c) {
+          uint32_t v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-          ptx::tmem_st32(tO + lane_base + c * 32, o);
+          for (int j = 0; j < 8; ++j) {
+            const uint4 x = h < a.H ? __ldg(qsrc + c * 8 + j) : make_uint4(0, 0, 0, 0);
+            v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+          }
+          ptx::tmem_st32(tmem + lane_base + c * 32, v);
         }
         ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(baddr(bars.q_ready));
       }
-      l *= f;
-      m_used = m_new;
-    }
-    float psum = 0.f;
-    uint32_t packed[kKT / 2];
+      const uint32_t peer_slots = ptx::map_to_rank(sbase + kOffSlots, 1);
+      uint8_t* stage = smem + kOffStage;
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true, range_err = false;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int sb = i % kSBufs;
+        // exits are taken by all 128 threads together (named barriers below are unbounded):
+        // a failed wait is voted on at the next barrier instead of breaking out alone
+        const bool got = __all_sync(
+            0xffffffffu, ptx::mbar_wait(baddr(bars.s_full[sb]), (i / kSBufs) & 1, abort_flag, a.status, a.limit_ns));
+        uint32_t sr[32];
+        if (got) {
+          ptx::tc_fence_after();
+          ptx::tmem_ld32(tmem + kColS + sb * kKT + lane_base, sr);
+          ptx::tmem_wait_ld();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(baddr(bars.s_empty[sb]));
+        } else {
 #pragma unroll
-    for (int j = 0; j < kKT; j += 2) {
-      const float p0 = fast_exp2(x[j] - m_used), p1 = fast_exp2(x[j + 1] - m_used);
-      psum += p0 + p1;
-      packed[j / 2] = pack_bf16(p0, p1);
-    }
-    l += psum;
-    // P row h: 64 bytes = 4 chunks of 16 B, 64B swizzle (chunk c lands at c ^ ((h >> 1) & 3))
+          for (int j = 0; j < 32; ++j) sr[j] = 0;
+        }
+        // which of the 32 keys are real (empty / out-of-range slots are masked)
+        const int slot = i * kKT + lane;
+        const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
+        const uint32_t vmask = __ballot_sync(0xffffffffu, latent_row(a, t, sidx, &range_err) >= 0);
+        float x[kKT];
+        float mt = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint4 val = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-      *reinterpret_cast<uint4*>(pP + h * 64 + ((c ^ ((h >> 1) & 3)) << 4)) = val;
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-
-    // ---- O += P V over this value half (V read MN-major from the gathered rows)
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      const uint32_t vbase = sKV + (v * (kHalf / 64)) * kKVBlockBytes;
+        for (int j = 0; j < kKT; ++j) {
+          x[j] = ((vmask >> j) & 1u) ? __uint_as_float(sr[j]) * a.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[j]);
+        }
+        const float m_new = fmaxf(m_used, mt);
+        const bool need = (i == 0) || (m_new > m_used + kRescaleThreshold);
+        const bool moved = __any_sync(0xffffffffu, need);
+        float fac = 1.f;
+        if (moved) {
+          fac = (i == 0) ? 0.f : fast_exp2(m_used - m_new);
+          l *= fac;
+          m_used = m_new;
+        }
+        float psum = 0.f;
+        uint32_t packed[kKT / 2];
 #pragma unroll
-      for (int ks = 0; ks < kKT / 16; ++ks) {
-        const uint64_t db = ptx::smem_desc(vbase + ks * 16 * 128, kKVBlockBytes, 1024, ptx::kLayoutSw128);
-        ptx::mma_bf16(tO, descP + 2 * ks, db, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+        for (int j = 0; j < kKT; j += 2) {
+          const float p0 = fast_exp2(x[j] - m_used), p1 = fast_exp2(x[j + 1] - m_used);
+          psum += p0 + p1;
+          packed[j / 2] = pack_bf16(p0, p1);
+        }
+        l += psum;
+        // staging buffer i % 2 is free once the bulk copy of tile i - 2 has read it
+        const int sbuf = i & 1;
+        if (h == 0) ptx::bulk_wait_read<1>();
+        if (ptx::named_sync_or(1, 128, !got || *abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sp = stage + sbuf * kSlotStride;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(sp + h * 64 + ((c ^ ((h >> 1) & 3)) << 4)) =
+              make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        reinterpret_cast<float*>(sp + kSlotFac)[h] = (moved && i > 0) ? fac : 1.f;
+        if (lane == 0) reinterpret_cast<int*>(sp + kSlotFlag)[warp & 3] = (moved && i > 0) ? 1 : 0;
+        ptx::fence_proxy_async_smem();
+        ptx::named_sync(2, 128);
+        if (h == 0) {
+          const int ps = i % kSlots;
+          if (!ptx::mbar_wait(baddr(bars.p_empty[ps]), ((i / kSlots) & 1) ^ 1, abort_flag, a.status, a.limit_ns)) {
+            ok = false;
+          } else {
+            ptx::bulk_copy_to_cluster(peer_slots + ps * kSlotStride, ptx::smem_addr(sp), kSlotBytes,
+                                      ptx::map_to_rank(baddr(bars.p_full[ps]), 1));
+            ptx::bulk_commit();
+          }
+        }
       }
-      ptx::mma_commit(bar_o);
+      if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
+      if (n_tiles > 0) {
+        // final row statistics for rank 1's normalisation
+        if (h == 0) ptx::bulk_wait_read<0>();
+        ptx::named_sync(1, 128);
+        float* st = reinterpret_cast<float*>(stage);
+        st[h] = l;
+        st[128 + h] = m_used;
+        ptx::fence_proxy_async_smem();
+        ptx::named_sync(2, 128);
+        if (h == 0 && ok) {
+          ptx::bulk_copy_to_cluster(ptx::map_to_rank(sbase + kOffStats, 1), ptx::smem_addr(stage), kStatsBytes,
+                                    ptx::map_to_rank(baddr(bars.stats_full), 1));
+          ptx::bulk_commit();
+        }
+        if (h == 0) ptx::bulk_wait_read<0>();
+      }
+      if (a.lse != nullptr && h < a.H)
+        a.lse[static_cast<int64_t>(t) * a.H + h] =
+            (ok && n_tiles > 0) ? (m_used + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
     }
-    if (!ptx::mbar_wait(bar_o, phase_o, abort_flag, a.status, a.limit_ns)) { ok = false; break; }
-    phase_o ^= 1;
-    ptx::tc_fence_after();
-  }
-  ptx::cp_async_wait<0>();
-  if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
-
-  // ---- epilogue: O / l -> bf16
-  const bool has_rows = n_tiles > 0 && ok;
-  const float inv_l = (has_rows && l > 0.f) ? 1.f / l : 0.f;
-  uint16_t* orow = a.out + (static_cast<int64_t>(t) * a.H + h) * kDV + v * kHalf;
+  } else {
+    // ================================================================ value CTA
+    if (warp == 0) {
+      if (lane == 0 && n_tiles > 0) {
+        constexpr uint32_t kIdescPV = ptx::instr_desc(128, 256, 1, 1, 0, 1);
+        for (int i = 0; i < n_tiles; ++i) {
+          const int vs = i % kVStages, ps = i % kSlots;
+          if (!ptx::mbar_wait(baddr(bars.v_full[vs]), (i / kVStages) & 1, abort_flag, a.status, a.limit_ns) ||
+              !ptx::mbar_wait(baddr(bars.ready[ps]), (i / kSlots) & 1, abort_flag, a.status, a.limit_ns))
+            break;
+          ptx::tc_fence_after();
+          const uint32_t vst = sbase + kOffV + vs * kVStageBytes;
+          const uint64_t da = ptx::smem_desc(sbase + kOffSlots + ps * kSlotStride, 16, 512, ptx::kLayoutSw64);
+#pragma unroll
+          for (int ks = 0; ks < kKT / 16; ++ks) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const uint64_t db =
+                  ptx::smem_desc(vst + half * 4 * kBlockBytes + ks * 16 * 128, kBlockBytes, 1024, ptx::kLayoutSw128);
+              ptx::mma_bf16(tmem + half * 256, da + 2 * ks, db, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(baddr(bars.v_empty[vs]));
+          ptx::mma_commit(baddr(bars.slot_free[ps]));
+        }
+        ptx::mma_commit(baddr(bars.mma_done));
+        drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
+      }
+    } else if (warp <= kProdWarps) {
+      producer_loop(a, t, idx_row, n_tiles, sbase + kOffV, kVStageBytes, kVStages, 8, bars.v_full, bars.v_empty,
+                    abort_flag);
+    } else if (warp < kCreditWarp) {
+      // ------------------------------------------------------------ rescale, then epilogue
+      const int h = (warp & 3) * 32 + lane;
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      bool ok = true;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int ps = i % kSlots;
+        if (!__all_sync(0xffffffffu,
+                        ptx::mbar_wait(baddr(bars.p_full[ps]), (i / kSlots) & 1, abort_flag, a.status, a.limit_ns))) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sp = smem + kOffSlots + ps * kSlotStride;
+        if (reinterpret_cast<const volatile int*>(sp + kSlotFlag)[warp & 3]) {
+          // rank 0 moved this warp's running max: O must include PV(i-1) before it is rescaled
+          const int j = i - 1;
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(baddr(bars.slot_free[j % kSlots]), (j / kSlots) & 1,
+                                                      abort_flag, a.status, a.limit_ns))) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const float f = reinterpret_cast<const float*>(sp + kSlotFac)[h];
 #pragma unroll 1
-  for (int c = 0; c < kHalf / 32; ++c) {
-    uint32_t o[32];
-    ptx::tmem_ld32(tO + lane_base + c * 32, o);
-    ptx::tmem_wait_ld();
-    if (h < a.H) {
-      uint32_t pk[16];
+          for (int c = 0; c < 16; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tmem + lane_base + c * 32, o);
+            ptx::tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        pk[j] = has_rows ? pack_bf16(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l) : 0u;
-      uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            ptx::tmem_st32(tmem + lane_base + c * 32, o);
+          }
+          ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(baddr(bars.ready[ps]));
+      }
+      // ---- epilogue: O / l -> bf16
+      float inv_l = 0.f;
+      if (ok && n_tiles > 0) {
+        const int j = n_tiles - 1;
+        ok = ptx::mbar_wait(baddr(bars.stats_full), 0, abort_flag, a.status, a.limit_ns) &&
+             ptx::mbar_wait(baddr(bars.slot_free[j % kSlots]), (j / kSlots) & 1, abort_flag, a.status, a.limit_ns);
+        const float l = reinterpret_cast<const float*>(smem + kOffStats)[h];
+        inv_l = (ok && l > 0.f) ? 1.f / l : 0.f;
+      }
+      ptx::tc_fence_after();
+      const bool has_rows = ok && n_tiles > 0;
+      uint16_t* orow = a.out + (static_cast<int64_t>(t) * a.H + h) * kDV;
+#pragma unroll 1
+      for (int c = 0; c < 16; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tmem + lane_base + c * 32, o);
+        ptx::tmem_wait_ld();
+        if (h < a.H) {
+          uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          for (int e = 0; e < 16; ++e)
+            pk[e] = has_rows ? pack_bf16(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l)
+                             : 0u;
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    } else if (lane == 0) {
+      // ------------------------------------------------------------ slot credits back to rank 0
+      for (int i = 0; i < n_tiles; ++i) {
+        const int ps = i % kSlots;
+        if (!ptx::mbar_wait(baddr(bars.slot_free[ps]), (i / kSlots) & 1, abort_flag, a.status, a.limit_ns)) break;
+        if (i + kSlots < n_tiles) {
+          ptx::mbar_arrive_expect_tx(baddr(bars.p_full[ps]), kSlotBytes);
+          ptx::mbar_arrive_cluster(ptx::map_to_rank(baddr(bars.p_empty[ps]), 0));
+        }
+      }
     }
   }
-  if (v == 0 && a.lse != nullptr && h < a.H)
-    a.lse[static_cast<int64_t>(t) * a.H + h] =
-        has_rows ? (m_used + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
 
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync_all();  // no remote access into either CTA's shared memory after this point
   if (warp == 0) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
@@ -296,7 +499,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<dim3(a.T, 2), kThreads, kSmem, stream>>>(a);
+  sparse_attn_kernel<<<dim3(2 * a.T), kThreads, kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
