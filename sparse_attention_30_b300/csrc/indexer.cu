@@ -9,7 +9,7 @@
 //
 // Warp roles (320 threads):
 //   warp 0      TMA producer: the query tile once, then key tiles through a ring of stages
-//   warp 1      owns TMEM; one lane issues the FP8 MMAs (K = 128 as 4 x K32)
+//   warp 1      owns TMEM and issues the FP8 MMAs (K = 128 as 4 x K32), one elected lane
 //   warps 2..9  two epilogue groups of 4 warps; group g drains TMEM buffer g (tiles i = g mod 2):
 //               ReLU, weight, sum over heads, key scale, causal mask, store fp32 scores.
 #include "dsa_internal.h"
@@ -183,31 +183,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdesc = ptx::instr_desc(kTileKeys, C::NCOL, 0, 0, 0, 0);
-      const uint64_t bdesc = ptx::smem_desc(sQ, 16, 1024, ptx::kLayoutSw128);
-      if (ptx::mbar_wait(q_full(), 0, abort_flag, a.status, a.limit_ns)) {
-        for (int i = 0; i < n_tiles; ++i) {
-          const int st = i % C::STAGES;
-          const uint32_t ph = (i / C::STAGES) & 1;
-          const int buf = i & 1;
-          const uint32_t bph = (i >> 1) & 1;
-          if (!ptx::mbar_wait(k_full(st), ph, abort_flag, a.status, a.limit_ns)) break;
-          if (!ptx::mbar_wait(t_empty(buf), bph ^ 1, abort_flag, a.status, a.limit_ns)) break;
-          ptx::tc_fence_after();
-          const uint64_t adesc = ptx::smem_desc(sK + st * kKeyTileBytes, 16, 1024, ptx::kLayoutSw128);
-          const uint32_t d = tmem + buf * C::NCOL;
+    // ------------------------------------------------ MMA issuer (whole warp, one elected lane)
+    constexpr uint32_t kIdesc = ptx::instr_desc(kTileKeys, C::NCOL, 0, 0, 0, 0);
+    const uint64_t bdesc = ptx::smem_desc(sQ, 16, 1024, ptx::kLayoutSw128);
+    auto wwait = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, a.status, a.limit_ns));
+    };
+    if (wwait(q_full(), 0)) {
+      for (int i = 0; i < n_tiles; ++i) {
+        const int st = i % C::STAGES;
+        const uint32_t ph = (i / C::STAGES) & 1;
+        const int buf = i & 1;
+        const uint32_t bph = (i >> 1) & 1;
+        if (!wwait(k_full(st), ph)) break;
+        if (!wwait(t_empty(buf), bph ^ 1)) break;
+        ptx::tc_fence_after();
+        const uint64_t adesc = ptx::smem_desc(sK + st * kKeyTileBytes, 16, 1024, ptx::kLayoutSw128);
+        const uint32_t d = tmem + buf * C::NCOL;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // K = 128 bytes = 4 x 32 FP8 values; +32 B = +2 in the descriptor
-            ptx::mma_f8(d, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
-          ptx::mma_commit(k_empty(st));
-          ptx::mma_commit(t_full(buf));
-        }
+        for (int kk = 0; kk < 4; ++kk)  // K = 128 bytes = 4 x 32 FP8 values; +32 B = +2 in the descriptor
+          ptx::mma_f8_warp(d, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+        ptx::mma_commit_warp(k_empty(st));
+        ptx::mma_commit_warp(t_full(buf));
       }
-      ptx::mma_commit(mma_done);
-      drain_wait(mma_done, 0, a.limit_ns);
     }
+    ptx::mma_commit_warp(mma_done);
+    drain_wait(mma_done, 0, a.limit_ns);
   } else {
     // ------------------------------------------------ epilogue
     const int g = (warp - 2) >> 2;  // tiles i = g mod 2 use TMEM buffer g

@@ -7,18 +7,21 @@
 // One token runs on a cluster of two CTAs with different jobs, and data flows one way:
 //
 //   rank 0, "score" CTA: Q [128 x 576] bf16 sits in TMEM (A operand of the MMA read straight
-//     from tensor memory), S = Q K^T is computed 32 keys at a time into four TMEM buffers from
-//     K rows gathered by eight cp.async warps into a 5-stage shared-memory ring, and four warps
-//     (one head row per thread) run the online softmax.  Each 32-key tile of P (bf16) plus per-row rescale factors is
-//     pushed into rank 1's shared memory with an asynchronous bulk copy.
-//   rank 1, "value" CTA: O [128 x 512] fp32 fills its whole TMEM; eight warps gather the value
-//     part (first 512 latent dims) of the same rows into a 4-stage ring and it runs O += P V as soon
-//     as a P tile lands.  When rank 0 moved a row's running max (lazily: only when it grows
-//     by more than 2^8), the factor travels with P and O is rescaled before that tile's PV.
-//     Ring slots are handed back to rank 0 by a credit warp, off the critical path.
+//     from tensor memory); S = Q K^T is computed 64 keys at a time (N = 64) into two TMEM
+//     buffers from K rows that twelve cp.async warps gather into a 2-stage ring; four warps
+//     (one head row per thread) run the online softmax.  Each 64-key tile of P (bf16) plus
+//     per-row rescale factors is pushed into rank 1's shared memory with an asynchronous bulk
+//     copy.
+//   rank 1, "value" CTA: O [128 x 512] fp32 fills its whole TMEM; twelve warps gather the value
+//     part (first 512 latent dims) of the same rows into a 2-stage ring and O += P V runs as soon
+//     as a P tile lands.  When rank 0 moved a row's running max (lazily: only when it grows by
+//     more than 2^8), the factor travels with P and O is rescaled before that tile's PV.  Ring
+//     slots are handed back to rank 0 by a credit warp, off the critical path.
 //
-// Nothing is computed twice and nothing waits on a round trip between the CTAs; the MMA
-// work is 576 (S) vs 512 (PV) latent dims per key on the two SMs.
+// Nothing is computed twice and nothing waits on a round trip between the CTAs; the MMA work is
+// 576 (S) vs 512 (PV) latent dims per key on the two SMs.  MMAs are issued warp-uniformly
+// (one elected lane), and tiles are 64 keys wide, because narrow or single-thread-issued
+// tcgen05.mma chains are issue-bound rather than tensor-bound.
 #include <cuda_bf16.h>
 
 #include "dsa_internal.h"
@@ -27,24 +30,23 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 448;                  // 14 warps
-constexpr int kProdWarps = 8;                  // warps 1-8 gather
+constexpr int kProdWarps = 12;                 // warps 1..12 gather
 constexpr int kProducers = kProdWarps * 32;
-constexpr int kRowWarp0 = 1 + kProdWarps;      // warps 9-12: one head row per thread (TMEM lane)
-constexpr int kCreditWarp = kRowWarp0 + 4;     // warp 13 (rank 1): slot credits
-constexpr int kKT = 32;                        // keys per tile
+constexpr int kRowWarp0 = 1 + kProdWarps;      // warps 13..16: one head row per thread (TMEM lane)
+constexpr int kCreditWarp = kRowWarp0 + 4;     // warp 17 (rank 1): slot credits
+constexpr int kThreads = 32 * (kCreditWarp + 1);
+constexpr int kKT = 64;                        // keys per tile
 constexpr int kDL = 576, kDV = 512;
-constexpr int kKStages = 5, kVStages = 4, kSlots = 6, kSBufs = 4;
-constexpr int kLag = 2;                        // gather signals tile i - kLag after issuing tile i
-constexpr int kBlockBytes = kKT * 128;         // 32 rows x 64 bf16
-constexpr int kKStageBytes = 9 * kBlockBytes;  // 36 KB: all 576 dims
-constexpr int kVStageBytes = 8 * kBlockBytes;  // 32 KB: value dims 0..511
-// P slot: P [128 x 32] bf16 (64B-swizzled) | 128 fp32 factors | 4 int flags (one per row warp)
+constexpr int kKStages = 2, kVStages = 2, kSlots = 4, kSBufs = 2;
+constexpr int kBlockBytes = kKT * 128;         // 64 rows x 64 bf16
+constexpr int kKStageBytes = 9 * kBlockBytes;  // 72 KB: all 576 dims
+constexpr int kVStageBytes = 8 * kBlockBytes;  // 64 KB: value dims 0..511
+// P slot: P [128 x 64] bf16 (128B-swizzled) | 128 fp32 factors | 4 int flags (one per row warp)
 constexpr int kSlotP = 128 * kKT * 2;
 constexpr int kSlotFac = kSlotP;
 constexpr int kSlotFlag = kSlotFac + 128 * 4;
 constexpr int kSlotBytes = kSlotFlag + 16;     // bytes moved per tile
-constexpr int kSlotStride = 9216;
+constexpr int kSlotStride = 17408;
 constexpr int kStatsBytes = 1024;              // l[128], m[128]
 // rank 0 layout
 constexpr int kOffK = 0;
@@ -59,6 +61,7 @@ constexpr int kSmem = (kEnd0 > kEnd1 ? kEnd0 : kEnd1) + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 288;                // rank 0: Q in columns 0..287, S buffers after it
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
+static_assert(kColS + kSBufs * kKT <= kTmemCols, "rank 0 TMEM budget");
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -102,62 +105,61 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-// Gather of tile i: `nblk` 64-dim blocks (from latent dim 0) of each of the 32 selected rows
-// into a 128B-swizzled stage.  Each producer warp copies whole rows (rows w, w + 8, ...): the
-// tile's 32 positions are read once (one per lane) and the row addresses are broadcast with
-// shuffles, so no load sits between consecutive copies; lanes move consecutive 16-byte chunks.
+// Warp-uniform bounded wait (all lanes agree on the outcome).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, const AttnArgs& a) {
+  return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, a.status, a.limit_ns));
+}
+
+// Gather of tile i: `nblk` 64-dim blocks (from latent dim 0) of each of the 64 selected rows into
+// a 128B-swizzled stage.  Producer warp pw copies whole rows pw, pw + 12, ...: the tile's positions
+// are read once (two per lane) and row addresses are broadcast with shuffles, so no load sits
+// between consecutive copies; the lanes move consecutive 16-byte chunks of a row.
 __device__ __forceinline__ void gather_rows(const AttnArgs& a, int t, const int32_t* idx_row, int i, uint32_t dst,
                                             int nblk, int pw, int lane, bool* range_err) {
-  const int slot = i * kKT + lane;
-  const int32_t s = slot < a.k ? __ldg(idx_row + slot) : -1;
-  const int64_t pr = latent_row(a, t, s, range_err);
-  const uint16_t* base = a.kv + (pr < 0 ? 0 : pr * kDL);
+  const uint16_t* base[2];
+  bool ok[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int slot = i * kKT + h * 32 + lane;
+    const int32_t s = slot < a.k ? __ldg(idx_row + slot) : -1;
+    const int64_t pr = latent_row(a, t, s, range_err);
+    base[h] = a.kv + (pr < 0 ? 0 : pr * kDL);
+    ok[h] = pr >= 0;
+  }
   const int chunks = nblk * 8;
   for (int r = pw; r < kKT; r += kProdWarps) {
+    const int h = r >> 5;
     const uint16_t* src = reinterpret_cast<const uint16_t*>(
-        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(base), r));
-    const bool ok = __shfl_sync(0xffffffffu, pr >= 0 ? 1 : 0, r) != 0;
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(h ? base[1] : base[0]), r & 31));
+    const bool okr = __shfl_sync(0xffffffffu, (h ? ok[1] : ok[0]) ? 1 : 0, r & 31) != 0;
     const uint32_t drow = dst + r * 128;
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
       const int cc = lane + 32 * j;
       if (cc < chunks) {
         const int blk = cc >> 3, c = cc & 7;
-        ptx::cp_async16(drow + blk * kBlockBytes + ((c ^ (r & 7)) << 4), src + cc * 8, ok);
+        ptx::cp_async16(drow + blk * kBlockBytes + ((c ^ (r & 7)) << 4), src + cc * 8, okr);
       }
     }
   }
 }
 
-// Producer loop shared by both ranks: ring of `stages` stages, signalling with a lag of kLag.
+// Producer loop shared by both ranks: ring of `stages` stages.  Completion of a stage is tracked
+// by the hardware (each producer thread's cp.async copies arrive on the stage's barrier when they
+// land), so producers never wait for their own copies and move straight on to the next stage.
+// The consumer issues fence.proxy.async after the barrier before the tensor core reads the stage.
 __device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const int32_t* idx_row, int n_tiles,
                                               uint32_t ring, int stage_bytes, int stages, int nblk,
                                               uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
   const int pw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
   bool range_err = false;
-  int issued = 0;
   for (int i = 0; i < n_tiles; ++i) {
     const int st = i % stages;
-    if (!__all_sync(0xffffffffu, ptx::mbar_wait(baddr(empty[st]), ((i / stages) & 1) ^ 1, abort_flag, a.status,
-                                                a.limit_ns)))
-      break;
+    if (!warp_wait(baddr(empty[st]), ((i / stages) & 1) ^ 1, abort_flag, a)) break;
     gather_rows(a, t, idx_row, i, ring + st * stage_bytes, nblk, pw, lane, &range_err);
-    ptx::cp_async_commit();
-    ++issued;
-    if (i >= kLag) {
-      ptx::cp_async_wait<kLag>();
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(baddr(full[(i - kLag) % stages]));
-    }
+    ptx::cp_async_arrive_noinc(baddr(full[st]));
   }
-  if (issued >= 2) {
-    ptx::cp_async_wait<1>();
-    ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive(baddr(full[(issued - 2) % stages]));
-  }
-  ptx::cp_async_wait<0>();
-  ptx::fence_proxy_async_smem();
-  if (issued >= 1) ptx::mbar_arrive(baddr(full[(issued - 1) % stages]));
+  ptx::cp_async_wait<0>();  // nothing of this thread's may still be in flight when the CTA exits
   if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
 }
 
@@ -231,27 +233,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
   if (rank == 0) {
     // ================================================================ score CTA
     if (warp == 0) {
-      if (lane == 0 && n_tiles > 0) {
+      if (n_tiles > 0) {
+        // ---- S = Q K^T, issued by the whole warp (one elected lane)
         constexpr uint32_t kIdescS = ptx::instr_desc(128, kKT, 1, 1, 0, 0);
-        bool ok = ptx::mbar_wait(baddr(bars.q_ready), 0, abort_flag, a.status, a.limit_ns);
+        bool ok = warp_wait(baddr(bars.q_ready), 0, abort_flag, a);
         ptx::tc_fence_after();
         for (int i = 0; ok && i < n_tiles; ++i) {
           const int st = i % kKStages, sb = i % kSBufs;
-          if (!ptx::mbar_wait(baddr(bars.k_full[st]), (i / kKStages) & 1, abort_flag, a.status, a.limit_ns) ||
-              !ptx::mbar_wait(baddr(bars.s_empty[sb]), ((i / kSBufs) & 1) ^ 1, abort_flag, a.status,
-                              a.limit_ns))
+          if (!warp_wait(baddr(bars.k_full[st]), (i / kKStages) & 1, abort_flag, a) ||
+              !warp_wait(baddr(bars.s_empty[sb]), ((i / kSBufs) & 1) ^ 1, abort_flag, a))
             break;
+          ptx::fence_proxy_async_smem();  // gathered rows (generic-proxy writes) -> tensor-core reads
           ptx::tc_fence_after();
           const uint64_t db0 = ptx::smem_desc(sbase + kOffK + st * kKStageBytes, 16, 1024, ptx::kLayoutSw128);
           const uint32_t d = tmem + kColS + sb * kKT;
 #pragma unroll
           for (int f = 0; f < 36; ++f)  // K = 576 = 36 x 16; A step = 8 TMEM columns, B step = 32 bytes
-            ptx::mma_bf16_ts(d, tmem + f * 8, db0 + (f >> 2) * (kBlockBytes >> 4) + 2 * (f & 3), kIdescS,
-                             f > 0 ? 1u : 0u);
-          ptx::mma_commit(baddr(bars.k_empty[st]));
-          ptx::mma_commit(baddr(bars.s_full[sb]));
+            ptx::mma_bf16_ts_warp(d, tmem + f * 8, db0 + (f >> 2) * (kBlockBytes >> 4) + 2 * (f & 3), kIdescS,
+                                  f > 0 ? 1u : 0u);
+          ptx::mma_commit_warp(baddr(bars.k_empty[st]));
+          ptx::mma_commit_warp(baddr(bars.s_full[sb]));
         }
-        ptx::mma_commit(baddr(bars.mma_done));
+        ptx::mma_commit_warp(baddr(bars.mma_done));
         drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
       }
     } else if (warp <= kProdWarps) {
@@ -285,28 +288,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         const int sb = i % kSBufs;
         // exits are taken by all 128 threads together (named barriers below are unbounded):
         // a failed wait is voted on at the next barrier instead of breaking out alone
-        const bool got = __all_sync(
-            0xffffffffu, ptx::mbar_wait(baddr(bars.s_full[sb]), (i / kSBufs) & 1, abort_flag, a.status, a.limit_ns));
-        uint32_t sr[32];
+        const bool got = warp_wait(baddr(bars.s_full[sb]), (i / kSBufs) & 1, abort_flag, a);
+        uint32_t s0[32], s1[32];
         if (got) {
           ptx::tc_fence_after();
-          ptx::tmem_ld32(tmem + kColS + sb * kKT + lane_base, sr);
+          ptx::tmem_ld32(tmem + kColS + sb * kKT + lane_base, s0);
+          ptx::tmem_ld32(tmem + kColS + sb * kKT + 32 + lane_base, s1);
           ptx::tmem_wait_ld();
           ptx::tc_fence_before();
           ptx::mbar_arrive(baddr(bars.s_empty[sb]));
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sr[j] = 0;
+          for (int j = 0; j < 32; ++j) s0[j] = s1[j] = 0;
         }
-        // which of the 32 keys are real (empty / out-of-range slots are masked)
-        const int slot = i * kKT + lane;
-        const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
-        const uint32_t vmask = __ballot_sync(0xffffffffu, latent_row(a, t, sidx, &range_err) >= 0);
+        // which of the 64 keys are real (empty / out-of-range slots are masked)
+        uint32_t vm[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int slot = i * kKT + hh * 32 + lane;
+          const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
+          vm[hh] = __ballot_sync(0xffffffffu, latent_row(a, t, sidx, &range_err) >= 0);
+        }
         float x[kKT];
         float mt = -INFINITY;
 #pragma unroll
         for (int j = 0; j < kKT; ++j) {
-          x[j] = ((vmask >> j) & 1u) ? __uint_as_float(sr[j]) * a.scale_log2 : -INFINITY;
+          const uint32_t raw = j < 32 ? s0[j] : s1[j - 32];
+          x[j] = ((vm[j >> 5] >> (j & 31)) & 1u) ? __uint_as_float(raw) * a.scale_log2 : -INFINITY;
           mt = fmaxf(mt, x[j]);
         }
         const float m_new = fmaxf(m_used, mt);
@@ -335,9 +343,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
           break;
         }
         uint8_t* sp = stage + sbuf * kSlotStride;
+        // P row h: 128 bytes = 8 chunks of 16 B, 128B swizzle (chunk c lands at c ^ (h & 7))
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(sp + h * 64 + ((c ^ ((h >> 1) & 3)) << 4)) =
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(sp + h * 128 + ((c ^ (h & 7)) << 4)) =
               make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
         reinterpret_cast<float*>(sp + kSlotFac)[h] = (moved && i > 0) ? fac : 1.f;
         if (lane == 0) reinterpret_cast<int*>(sp + kSlotFlag)[warp & 3] = (moved && i > 0) ? 1 : 0;
@@ -378,29 +387,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
   } else {
     // ================================================================ value CTA
     if (warp == 0) {
-      if (lane == 0 && n_tiles > 0) {
+      if (n_tiles > 0) {
+        // ---- O += P V over two N = 256 halves, issued by the whole warp (one elected lane)
         constexpr uint32_t kIdescPV = ptx::instr_desc(128, 256, 1, 1, 0, 1);
         for (int i = 0; i < n_tiles; ++i) {
           const int vs = i % kVStages, ps = i % kSlots;
-          if (!ptx::mbar_wait(baddr(bars.v_full[vs]), (i / kVStages) & 1, abort_flag, a.status, a.limit_ns) ||
-              !ptx::mbar_wait(baddr(bars.ready[ps]), (i / kSlots) & 1, abort_flag, a.status, a.limit_ns))
+          if (!warp_wait(baddr(bars.v_full[vs]), (i / kVStages) & 1, abort_flag, a) ||
+              !warp_wait(baddr(bars.ready[ps]), (i / kSlots) & 1, abort_flag, a))
             break;
+          ptx::fence_proxy_async_smem();  // gathered rows (generic-proxy writes) -> tensor-core reads
           ptx::tc_fence_after();
           const uint32_t vst = sbase + kOffV + vs * kVStageBytes;
-          const uint64_t da = ptx::smem_desc(sbase + kOffSlots + ps * kSlotStride, 16, 512, ptx::kLayoutSw64);
+          const uint64_t da = ptx::smem_desc(sbase + kOffSlots + ps * kSlotStride, 16, 1024, ptx::kLayoutSw128);
 #pragma unroll
           for (int ks = 0; ks < kKT / 16; ++ks) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
+              // V rows ks*16 .. ks*16+15 of blocks 4*half .. 4*half+3, read MN-major
               const uint64_t db =
                   ptx::smem_desc(vst + half * 4 * kBlockBytes + ks * 16 * 128, kBlockBytes, 1024, ptx::kLayoutSw128);
-              ptx::mma_bf16(tmem + half * 256, da + 2 * ks, db, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+              ptx::mma_bf16_warp(tmem + half * 256, da + 2 * ks, db, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
             }
           }
-          ptx::mma_commit(baddr(bars.v_empty[vs]));
-          ptx::mma_commit(baddr(bars.slot_free[ps]));
+          ptx::mma_commit_warp(baddr(bars.v_empty[vs]));
+          ptx::mma_commit_warp(baddr(bars.slot_free[ps]));
         }
-        ptx::mma_commit(baddr(bars.mma_done));
+        ptx::mma_commit_warp(baddr(bars.mma_done));
         drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
       }
     } else if (warp <= kProdWarps) {
@@ -413,8 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
       bool ok = true;
       for (int i = 0; i < n_tiles; ++i) {
         const int ps = i % kSlots;
-        if (!__all_sync(0xffffffffu,
-                        ptx::mbar_wait(baddr(bars.p_full[ps]), (i / kSlots) & 1, abort_flag, a.status, a.limit_ns))) {
+        if (!warp_wait(baddr(bars.p_full[ps]), (i / kSlots) & 1, abort_flag, a)) {
           ok = false;
           break;
         }
@@ -422,8 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         if (reinterpret_cast<const volatile int*>(sp + kSlotFlag)[warp & 3]) {
           // rank 0 moved this warp's running max: O must include PV(i-1) before it is rescaled
           const int j = i - 1;
-          if (!__all_sync(0xffffffffu, ptx::mbar_wait(baddr(bars.slot_free[j % kSlots]), (j / kSlots) & 1,
-                                                      abort_flag, a.status, a.limit_ns))) {
+          if (!warp_wait(baddr(bars.slot_free[j % kSlots]), (j / kSlots) & 1, abort_flag, a)) {
             ok = false;
             break;
           }
