@@ -103,11 +103,23 @@ def _dist():
 
 
 def _max_over_ranks(dist, x: float) -> float:
+    """Max of x over all ranks (the step time the job is charged), NCCL or gloo."""
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank runs its own sequence of the same workload (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
+def aggregate_tokens_per_s(tokens_per_rank: int, world_size: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world_size * steps / (max_ms / 1e3)
 
 
 def _barrier(dist):
@@ -203,7 +215,7 @@ def run_ours(args, dist, rank, ws):
     cid = {"prefill128k": 4, "prefill4k": 2}[args.workload]
     cfg = synth.config(cid)
     if rank:
-        cfg = synth.config(cid, seed=cfg.seed + 1000 * rank)
+        cfg = synth.config(cid, seed=rank_seed(cfg.seed, rank))
     d = synth.prefill_inputs(cfg, device="cuda")
     runner = PrefillRunner(dsa, d, cfg, args.chunk)
 
@@ -227,8 +239,7 @@ def run_ours(args, dist, rank, ws):
     if st != 0:
         raise RuntimeError(f"device status {st} in the timed region")
     ms_step = total_ms / args.steps
-    tokens = cfg.L * ws * args.steps
-    value = tokens / (total_ms / 1e3)
+    value = aggregate_tokens_per_s(cfg.L, ws, args.steps, total_ms)
 
     # per-kernel rooflines (algorithmic work / summed launch time over the timed region)
     w = prefill_work(cfg.L, cfg.H_I, cfg.H, cfg.k)
