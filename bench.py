@@ -280,7 +280,8 @@ def run_ours(args, dist, rank, ws):
             "clocks": clk}
 
     if not args.no_decode:
-        line["decode"] = bench_decode(dsa, synth, args, peaks)
+        line["decode"] = bench_decode(dsa, synth, args, peaks, cid=5)
+        line["decode_b64_32k"] = bench_decode(dsa, synth, args, peaks, cid=3)
     if not args.no_e2e:
         line["e2e"] = bench_e2e(dsa, d, cfg, args)
     del d, runner
@@ -290,34 +291,71 @@ def run_ours(args, dist, rank, ws):
     return line
 
 
-def bench_decode(dsa, synth, args, peaks):
-    """Decode step (B=32, contexts ~U[8192,131072]) through dsa_forward; L2 flushed between steps."""
-    cfg = synth.config(5)
+def bench_decode(dsa, synth, args, peaks, cid=5):
+    """Decode step through dsa_forward (value) and stage by stage with CUDA events (breakdown);
+    L2 is flushed between steps."""
+    cfg = synth.config(cid)
     d = synth.decode_inputs(cfg, device="cuda")
     lens = d["seq_lens"].cpu().tolist()
     max_len = max(lens)
     f = dsa.Forward.decode(d, cfg.k, cfg.scale, max_len)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    ld = (max_len + 3) // 4 * 4
+    scores = torch.empty((cfg.B, ld), dtype=torch.float32, device="cuda")
+    idx = torch.empty((cfg.B, cfg.k), dtype=torch.int32, device="cuda")
+    out = torch.empty((cfg.B, cfg.H, 512), dtype=torch.bfloat16, device="cuda")
+
+    def stages(ev):
+        ev["index"].append(_rec())
+        dsa.index_paged(d["q8"], d["q_scale"], d["w"], d["k8_cache"], d["k_scale_cache"], d["block_table"],
+                        d["seq_lens"], max_len, scores=scores)
+        ev["index"].append(_rec())
+        ev["topk"].append(_rec())
+        dsa.topk(scores, cfg.k, row_lens=d["seq_lens"], idx=idx)
+        ev["topk"].append(_rec())
+        ev["attn"].append(_rec())
+        dsa.sparse_attn(d["q"], d["kv_cache"], idx, cfg.scale, block_table=d["block_table"], out=out, want_lse=False)
+        ev["attn"].append(_rec())
+
     for _ in range(max(3, args.warmup)):
         f()
-    times = []
-    for _ in range(max(10, args.steps)):
+        stages({"index": [], "topk": [], "attn": []})
+    n = max(10, args.steps)
+    times, ev = [], {"index": [], "topk": [], "attn": []}
+    for _ in range(n):
         flush.fill_(1.0)
         a = _rec()
         f()
         b = _rec()
         b.synchronize()
         times.append(a.elapsed_time(b))
+    for _ in range(n):
+        flush.fill_(1.0)
+        stages(ev)
+    torch.cuda.synchronize()
     st = dsa.device_status()
     if st != 0:
         raise RuntimeError(f"decode status {st}")
     ms = float(np.median(times))
     w = decode_work(lens, cfg.H_I, cfg.H, cfg.k)
+    kms = {k: _pairs_ms(v) / n for k, v in ev.items()}
+    kern = {
+        "indexer": dict(bound="hbm", ms=kms["index"], achieved=w["indexer_bytes"] / (kms["index"] * 1e-3) / 1e9,
+                        peak=peaks["hbm"], unit="GB/s"),
+        "topk": dict(bound="hbm", ms=kms["topk"], achieved=w["topk_bytes"] / (kms["topk"] * 1e-3) / 1e9,
+                     peak=peaks["hbm"], unit="GB/s"),
+        "sparse_attn": dict(bound="hbm", ms=kms["attn"], achieved=w["attn_bytes"] / (kms["attn"] * 1e-3) / 1e9,
+                            peak=peaks["hbm"], unit="GB/s"),
+    }
+    for v in kern.values():
+        v["frac"] = round(v["achieved"] / v["peak"], 4)
+        v["ms"] = round(v["ms"], 4)
+        v["achieved"] = round(v["achieved"], 1)
     tot_bytes = w["indexer_bytes"] + w["topk_bytes"] + w["attn_bytes"]
     return {"metric": "decode query-tok/s", "value": round(cfg.B / (ms * 1e-3), 1), "unit": "query-tok/s",
-            "ms_per_step": round(ms, 4), "workload": "mixed decode B=32, ctx~U[8192,131072], k=2048, H=128",
+            "ms_per_step": round(ms, 4), "workload": cfg.name + ", k=2048, H=128, H_I=64",
             "algorithmic_bytes": tot_bytes, "hbm_frac_of_step": round(tot_bytes / (ms * 1e-3) / 1e9 / peaks["hbm"], 4),
-            "l2": "flushed between steps (252 MB write)"}
+            "kernels": kern, "l2": "flushed between steps (252 MB write)"}
 
 
 def bench_e2e(dsa, d, cfg, args):

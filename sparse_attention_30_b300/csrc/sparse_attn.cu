@@ -112,34 +112,31 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 // Gather of tile i: `nblk` 64-dim blocks (from latent dim 0) of each of the 64 selected rows into
 // a 128B-swizzled stage.  Producer warp pw copies whole rows pw, pw + 12, ...: the tile's positions
-// are read once (two per lane) and row addresses are broadcast with shuffles, so no load sits
-// between consecutive copies; the lanes move consecutive 16-byte chunks of a row.
+// are read once (two per lane) and row addresses are broadcast with shuffles.  An empty or
+// out-of-range slot copies `fallback_row` instead (the token's first selected row, which is always
+// attended) so every copy is a plain 16-byte copy; the softmax masks that key to P = 0, so the
+// substitute never contributes.  The loop is kept minimal: the producers are issue-bound.
+template <int NBLK>
 __device__ __forceinline__ void gather_rows(const AttnArgs& a, int t, const int32_t* idx_row, int i, uint32_t dst,
-                                            int nblk, int pw, int lane, bool* range_err) {
+                                            int pw, int lane, int64_t fallback_row, bool* range_err) {
+  constexpr int kChunks = NBLK * 8;
   const uint16_t* base[2];
-  bool ok[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int slot = i * kKT + h * 32 + lane;
     const int32_t s = slot < a.k ? __ldg(idx_row + slot) : -1;
     const int64_t pr = latent_row(a, t, s, range_err);
-    base[h] = a.kv + (pr < 0 ? 0 : pr * kDL);
-    ok[h] = pr >= 0;
+    base[h] = a.kv + (pr < 0 ? fallback_row : pr) * kDL;
   }
-  const int chunks = nblk * 8;
   for (int r = pw; r < kKT; r += kProdWarps) {
-    const int h = r >> 5;
     const uint16_t* src = reinterpret_cast<const uint16_t*>(
-        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(h ? base[1] : base[0]), r & 31));
-    const bool okr = __shfl_sync(0xffffffffu, (h ? ok[1] : ok[0]) ? 1 : 0, r & 31) != 0;
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(r >> 5 ? base[1] : base[0]), r & 31));
     const uint32_t drow = dst + r * 128;
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
       const int cc = lane + 32 * j;
-      if (cc < chunks) {
-        const int blk = cc >> 3, c = cc & 7;
-        ptx::cp_async16(drow + blk * kBlockBytes + ((c ^ (r & 7)) << 4), src + cc * 8, okr);
-      }
+      if (cc < kChunks)
+        ptx::cp_async16_n<16>(drow + (cc >> 3) * kBlockBytes + (((cc & 7) ^ (r & 7)) << 4), src + cc * 8);
     }
   }
 }
@@ -148,15 +145,23 @@ __device__ __forceinline__ void gather_rows(const AttnArgs& a, int t, const int3
 // by the hardware (each producer thread's cp.async copies arrive on the stage's barrier when they
 // land), so producers never wait for their own copies and move straight on to the next stage.
 // The consumer issues fence.proxy.async after the barrier before the tensor core reads the stage.
+template <int NBLK>
 __device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const int32_t* idx_row, int n_tiles,
-                                              uint32_t ring, int stage_bytes, int stages, int nblk,
+                                              uint32_t ring, int stage_bytes, int stages,
                                               uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
   const int pw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
   bool range_err = false;
+  if (n_tiles <= 0) return;
+  // the first slot is valid whenever there is a tile (valid slots come first)
+  const int64_t fallback_row = latent_row(a, t, __ldg(idx_row), &range_err);
+  if (fallback_row < 0) {  // first position out of range: nothing safe to substitute
+    atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
+  }
   for (int i = 0; i < n_tiles; ++i) {
     const int st = i % stages;
     if (!warp_wait(baddr(empty[st]), ((i / stages) & 1) ^ 1, abort_flag, a)) break;
-    gather_rows(a, t, idx_row, i, ring + st * stage_bytes, nblk, pw, lane, &range_err);
+    gather_rows<NBLK>(a, t, idx_row, i, ring + st * stage_bytes, pw, lane, fallback_row < 0 ? 0 : fallback_row,
+                      &range_err);
     ptx::cp_async_arrive_noinc(baddr(full[st]));
   }
   ptx::cp_async_wait<0>();  // nothing of this thread's may still be in flight when the CTA exits
@@ -258,8 +263,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
       }
     } else if (warp <= kProdWarps) {
-      producer_loop(a, t, idx_row, n_tiles, sbase + kOffK, kKStageBytes, kKStages, 9, bars.k_full, bars.k_empty,
-                    abort_flag);
+      producer_loop<9>(a, t, idx_row, n_tiles, sbase + kOffK, kKStageBytes, kKStages, bars.k_full, bars.k_empty,
+                       abort_flag);
     } else if (warp < kCreditWarp) {
       // ------------------------------------------------------------ Q -> TMEM, then softmax
       const int h = (warp & 3) * 32 + lane;
@@ -416,8 +421,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
       }
     } else if (warp <= kProdWarps) {
-      producer_loop(a, t, idx_row, n_tiles, sbase + kOffV, kVStageBytes, kVStages, 8, bars.v_full, bars.v_empty,
-                    abort_flag);
+      producer_loop<8>(a, t, idx_row, n_tiles, sbase + kOffV, kVStageBytes, kVStages, bars.v_full, bars.v_empty,
+                       abort_flag);
     } else if (warp < kCreditWarp) {
       // ------------------------------------------------------------ rescale, then epilogue
       const int h = (warp & 3) * 32 + lane;
