@@ -212,6 +212,13 @@ def run_ours(args, dist, rank, ws):
     import sparse_attention_30_b300 as dsa
 
     peaks = _peaks()
+    if args.workload.startswith("decode"):
+        # decode-only run (used for profiler captures of the decode kernels)
+        res = bench_decode(dsa, synth, args, peaks, cid=5 if args.workload == "decode" else 3)
+        return {"metric": "decode query-tok/s", "value": res["value"], "unit": "query-tok/s", "n_gpus": ws,
+                "steps": max(10, args.steps), "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 / bf16",
+                "data": "synthetic", "config": {"workload": res["workload"]}, "decode": res}
     cid = {"prefill128k": 4, "prefill4k": 2}[args.workload]
     cfg = synth.config(cid)
     if rank:
@@ -304,6 +311,9 @@ def bench_decode(dsa, synth, args, peaks, cid=5):
     scores = torch.empty((cfg.B, ld), dtype=torch.float32, device="cuda")
     idx = torch.empty((cfg.B, cfg.k), dtype=torch.int32, device="cuda")
     out = torch.empty((cfg.B, cfg.H, 512), dtype=torch.bfloat16, device="cuda")
+    n_split = dsa.decode_split(cfg.B)
+    n_ws = dsa.lib.dsa_sparse_attn_split_workspace_size(cfg.B, cfg.H, n_split)
+    split_ws = torch.empty(n_ws, dtype=torch.uint8, device="cuda") if n_ws else None
 
     def stages(ev):
         ev["index"].append(_rec())
@@ -314,7 +324,8 @@ def bench_decode(dsa, synth, args, peaks, cid=5):
         dsa.topk(scores, cfg.k, row_lens=d["seq_lens"], idx=idx)
         ev["topk"].append(_rec())
         ev["attn"].append(_rec())
-        dsa.sparse_attn(d["q"], d["kv_cache"], idx, cfg.scale, block_table=d["block_table"], out=out, want_lse=False)
+        dsa.sparse_attn_split(d["q"], d["kv_cache"], idx, cfg.scale, n_split, block_table=d["block_table"], out=out,
+                              ws=split_ws)
         ev["attn"].append(_rec())
 
     for _ in range(max(3, args.warmup)):
@@ -483,8 +494,8 @@ def main():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--chunk", type=int, default=8192)
-    p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k"],
-                   help="prefill4k is the small case used for profiler captures")
+    p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k", "decode", "decode32k"],
+                   help="prefill4k / decode / decode32k run single pieces (used for profiler captures)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")

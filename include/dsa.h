@@ -145,6 +145,21 @@ dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv
                              const int32_t* idx, int T, int H, int k, float scale,
                              uint16_t* out, float* lse, dsa_stream_t stream);
 
+/*
+ * dsa_sparse_attn_split — dsa_sparse_attn with each row's selected keys spread over n_split
+ * independent partial attentions (a share of the slots each) that a second kernel merges
+ * exactly (log-sum-exp weights).  Same inputs, outputs and rules as dsa_sparse_attn; this is how
+ * the decode forward fills the GPU when it has few sequences.  `ws` is a caller-owned device
+ * buffer of dsa_sparse_attn_split_workspace_size(T, H, n_split) bytes (256-byte aligned) holding
+ * the partial outputs; n_split in [1, 8] (1 = dsa_sparse_attn, no workspace needed).
+ */
+size_t dsa_sparse_attn_split_workspace_size(int T, int H, int n_split);
+dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows,
+                                   const int32_t* block_table, int64_t bt_stride, int page_size,
+                                   const int32_t* idx, int T, int H, int k, float scale,
+                                   uint16_t* out, float* lse, int n_split, void* ws, size_t ws_bytes,
+                                   dsa_stream_t stream);
+
 /* Forward modes. */
 enum { DSA_MODE_PREFILL = 0, DSA_MODE_DECODE = 1 };
 

@@ -23,7 +23,8 @@ MODE_PREFILL, MODE_DECODE = 0, 1
 # Names of every function include/dsa.h declares.
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_index", "dsa_index_paged", "dsa_topk", "dsa_sparse_attn",
            "dsa_forward_workspace_size", "dsa_forward", "dsa_device_status", "dsa_selftest_wait_timeout",
-           "dsa_decode_noalloc", "dsa_decode_noalloc_capacity")
+           "dsa_decode_noalloc", "dsa_decode_noalloc_capacity", "dsa_sparse_attn_split_workspace_size",
+           "dsa_sparse_attn_split")
 
 
 class DSAError(RuntimeError):
@@ -70,6 +71,8 @@ def _load():
         "dsa_selftest_wait_timeout": ([I, P], I),
         "dsa_decode_noalloc": ([ctypes.POINTER(ForwardArgs), P], I),
         "dsa_decode_noalloc_capacity": ([], ctypes.c_size_t),
+        "dsa_sparse_attn_split_workspace_size": ([I, I, I], ctypes.c_size_t),
+        "dsa_sparse_attn_split": ([P, P, I64, P, I64, I, P, I, I, I, F, P, P, I, P, ctypes.c_size_t, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -173,6 +176,30 @@ def sparse_attn(q, kv, idx, scale, block_table=None, page_size=0, out=None, lse=
     bt_stride = block_table.stride(0) if block_table is not None else 0
     _check(lib.dsa_sparse_attn(_ptr(q), _ptr(kv), n_rows, _ptr(block_table), bt_stride, page_size, _ptr(idx), T, H,
                                k, float(scale), _ptr(out), _ptr(lse), _stream(q)), "dsa_sparse_attn")
+    return out, lse
+
+
+def decode_split(B: int) -> int:
+    """Key split the decode forward uses for B sequences (mirrors the library's choice)."""
+    return 1 if B <= 0 or B >= 74 else max(1, min(4, 74 // B))
+
+
+def sparse_attn_split(q, kv, idx, scale, n_split, block_table=None, out=None, lse=None, ws=None):
+    """dsa_sparse_attn_split: attention with each row's keys spread over n_split partial passes."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv, torch.bfloat16, "kv")
+    _need(idx, torch.int32, "idx", 2)
+    T, H, _ = q.shape
+    page_size = kv.shape[1] if block_table is not None else 0
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
+    n = lib.dsa_sparse_attn_split_workspace_size(T, H, n_split)
+    if ws is None and n:
+        ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    bt_stride = block_table.stride(0) if block_table is not None else 0
+    _check(lib.dsa_sparse_attn_split(_ptr(q), _ptr(kv), kv.numel() // 576, _ptr(block_table), bt_stride, page_size,
+                                     _ptr(idx), T, H, idx.shape[1], float(scale), _ptr(out), _ptr(lse), n_split,
+                                     _ptr(ws), 0 if ws is None else ws.numel(), _stream(q)), "dsa_sparse_attn_split")
     return out, lse
 
 

@@ -144,8 +144,16 @@ struct FwdPlan {
   int rows;          // query rows in total
   int chunk;         // rows scored per indexer / top-k launch
   int64_t ld;        // score row pitch (floats)
-  size_t scores_bytes, idx_bytes, total;
+  int n_split;       // decode: clusters per sequence in the attention (1 = no key split)
+  size_t scores_bytes, idx_bytes, part_o_bytes, part_ml_bytes, total;
 };
+
+// Decode attention runs one 2-SM cluster per sequence; with few sequences each one's selected
+// keys are split over several clusters so the 74 cluster slots of the GPU fill up.
+int decode_split(int B) {
+  if (B <= 0 || B >= 74) return 1;
+  return std::max(1, std::min(4, 74 / B));
+}
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -171,9 +179,13 @@ dsa_status_t plan_forward(const dsa_forward_args* a, FwdPlan* p) {
   } else {
     return DSA_ERR_INVALID_ARG;
   }
+  p->n_split = a->mode == DSA_MODE_DECODE ? decode_split(a->B) : 1;
   p->scores_bytes = align256(static_cast<size_t>(p->chunk) * p->ld * sizeof(float));
   p->idx_bytes = a->idx ? 0 : align256(static_cast<size_t>(std::max(1, p->rows)) * a->k * sizeof(int32_t));
-  p->total = p->scores_bytes + p->idx_bytes;
+  p->part_o_bytes = p->n_split > 1 ? align256(static_cast<size_t>(p->rows) * p->n_split * a->H * 512 * 4) : 0;
+  p->part_ml_bytes = p->n_split > 1 ? align256(static_cast<size_t>(p->rows) * p->n_split * a->H * 2 * 4) : 0;
+  // (same layout as dsa_sparse_attn_split's workspace: partial outputs, then partial max / sum)
+  p->total = p->scores_bytes + p->idx_bytes + p->part_o_bytes + p->part_ml_bytes;
   return DSA_OK;
 }
 
@@ -236,9 +248,11 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld, int T, const int32_t* row
   return from_cuda(launch_topk(a, stream));
 }
 
-dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* block_table,
-                             int64_t bt_stride, int page_size, const int32_t* idx, int T, int H, int k,
-                             float scale, uint16_t* out, float* lse, dsa_stream_t stream) {
+namespace {
+dsa_status_t sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* block_table,
+                               int64_t bt_stride, int page_size, const int32_t* idx, int T, int H, int k, float scale,
+                               uint16_t* out, float* lse, int n_split, float* part_o, float* part_ml,
+                               cudaStream_t stream) {
   dsa_status_t st = check_attn_args(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, out);
   if (st != DSA_OK || T == 0) return st;
   int* status = status_ptr();
@@ -248,7 +262,49 @@ dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv
   a.page_size = page_size; a.idx = idx; a.T = T; a.H = H; a.k = k;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = out; a.lse = lse; a.status = status; a.limit_ns = kWaitLimitNs;
+  a.n_split = n_split; a.part_o = part_o; a.part_ml = part_ml;
   return from_cuda(launch_sparse_attn(a, stream));
+}
+}  // namespace
+
+size_t split_part_o_bytes(int T, int H, int n_split) {
+  return align256(static_cast<size_t>(T) * n_split * H * 512 * 4);
+}
+size_t split_part_ml_bytes(int T, int H, int n_split) {
+  return align256(static_cast<size_t>(T) * n_split * H * 2 * 4);
+}
+
+extern "C" size_t dsa_sparse_attn_split_workspace_size(int T, int H, int n_split) {
+  if (T < 0 || H < 1 || H > 128 || n_split < 1 || n_split > 8) return 0;
+  if (n_split == 1) return 0;
+  return split_part_o_bytes(T, H, n_split) + split_part_ml_bytes(T, H, n_split);
+}
+
+extern "C" dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows,
+                                              const int32_t* block_table, int64_t bt_stride, int page_size,
+                                              const int32_t* idx, int T, int H, int k, float scale, uint16_t* out,
+                                              float* lse, int n_split, void* ws, size_t ws_bytes,
+                                              dsa_stream_t stream) {
+  if (n_split < 1 || n_split > 8) return DSA_ERR_INVALID_ARG;
+  if (n_split == 1)
+    return sparse_attn_split(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, scale, out, lse, 1,
+                             nullptr, nullptr, stream);
+  dsa_status_t st = check_attn_args(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, out);
+  if (st != DSA_OK || T == 0) return st;
+  const size_t need = dsa_sparse_attn_split_workspace_size(T, H, n_split);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
+  char* w = static_cast<char*>(ws);
+  return sparse_attn_split(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, scale, out, lse, n_split,
+                           reinterpret_cast<float*>(w), reinterpret_cast<float*>(w + split_part_o_bytes(T, H, n_split)),
+                           stream);
+}
+
+extern "C" dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows,
+                                        const int32_t* block_table, int64_t bt_stride, int page_size,
+                                        const int32_t* idx, int T, int H, int k, float scale, uint16_t* out,
+                                        float* lse, dsa_stream_t stream) {
+  return sparse_attn_split(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, scale, out, lse, 1,
+                           nullptr, nullptr, stream);
 }
 
 size_t dsa_forward_workspace_size(const dsa_forward_args* args) {
@@ -295,8 +351,11 @@ dsa_status_t dsa_forward(const dsa_forward_args* a, void* ws, size_t ws_bytes, d
   if (st != DSA_OK) return st;
   st = dsa_topk(scores, p.ld, a->B, a->seq_lens, p.ld, 0, a->k, idx, s);
   if (st != DSA_OK) return st;
-  return dsa_sparse_attn(a->q, a->kv, a->n_pages * a->page_size, a->block_table, a->bt_stride, a->page_size, idx,
-                         a->B, a->H, a->k, a->scale, a->out, a->lse, s);
+  char* part = static_cast<char*>(ws) + p.scores_bytes + p.idx_bytes;
+  return sparse_attn_split(a->q, a->kv, a->n_pages * a->page_size, a->block_table, a->bt_stride, a->page_size, idx,
+                           a->B, a->H, a->k, a->scale, a->out, a->lse, p.n_split,
+                           p.n_split > 1 ? reinterpret_cast<float*>(part) : nullptr,
+                           p.n_split > 1 ? reinterpret_cast<float*>(part + p.part_o_bytes) : nullptr, s);
 }
 
 dsa_status_t dsa_device_status(dsa_stream_t stream) {

@@ -68,8 +68,15 @@ struct AttnArgs {
   float* lse;                 // [T, H] or NULL
   int* status;
   uint64_t limit_ns;
+  // key split (decode with few sequences): n_split > 1 gives each token n_split clusters, each
+  // over a contiguous share of its selected tiles, writing partial results that
+  // launch_attn_combine merges into out / lse
+  int n_split;
+  float* part_o;              // [T, n_split, H, 512] fp32, each normalised by its own sum
+  float* part_ml;             // [T, n_split, H, 2] fp32: running max (log2 domain) and sum
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- self test
 

@@ -214,24 +214,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = (warp - 2) >> 2;  // tiles i = g mod 2 use TMEM buffer g
     const int sub = warp & 3;       // this warp may touch TMEM lanes [32*sub, 32*sub + 32)
     const int row = sub * 32 + lane;
+    // This group handles tiles g, g+2, g+4, ...  The key's page entry (decode) is fetched four tiles
+    // ahead and its scale two tiles ahead, so neither dependent load stalls the tile being finished.
+    auto key_of = [&](int i) { return (tb + i) * kTileKeys + row; };
+    auto page_of = [&](int i) -> int32_t {  // physical page of this thread's key in tile i, or -1
+      const int s = key_of(i);
+      if (i >= n_tiles || s >= key_end) return -1;
+      const int32_t phys = a.block_table[static_cast<int64_t>(row0) * a.bt_stride + s / a.page_size];
+      return (phys >= 0 && phys < a.n_pages) ? phys : -1;
+    };
+    auto scale_of = [&](int i, int32_t phys) -> float {  // 0 marks an invalid key
+      const int s = key_of(i);
+      if (i >= n_tiles || s >= key_end) return 0.f;
+      if (PAGED) return phys < 0 ? 0.f : a.k_scale[static_cast<int64_t>(phys) * a.page_size + s % a.page_size];
+      return a.k_scale[s];
+    };
+    int32_t page_a = PAGED ? page_of(g) : 0, page_b = PAGED ? page_of(g + 2) : 0;
+    float sk_next = PAGED ? scale_of(g, page_a) : 0.f;
     for (int i = g; i < n_tiles; i += 2) {
+      // prefill: one contiguous scale load per key (cheap, issued here); decode: pipelined lookups
+      const float sk = PAGED ? sk_next : scale_of(i, 0);
+      const bool kvalid = key_of(i) < key_end && (!PAGED || page_a >= 0);
+      if (PAGED) {
+        const int32_t page_c = page_of(i + 4);
+        sk_next = scale_of(i + 2, page_b);
+        page_a = page_b;
+        page_b = page_c;
+      }
+      const int s = key_of(i);
       const uint32_t bph = (i >> 1) & 1;
       if (!ptx::mbar_wait(t_full(g), bph, abort_flag, a.status, a.limit_ns)) break;
       ptx::tc_fence_after();
-      const int s = (tb + i) * kTileKeys + row;
-      bool kvalid = s < key_end;
-      float sk = 0.f;
-      if (kvalid) {
-        if (PAGED) {
-          const int32_t phys = a.block_table[static_cast<int64_t>(row0) * a.bt_stride + s / a.page_size];
-          if (phys >= 0 && phys < a.n_pages)
-            sk = a.k_scale[static_cast<int64_t>(phys) * a.page_size + s % a.page_size];
-          else
-            kvalid = false;
-        } else {
-          sk = a.k_scale[s];
-        }
-      }
       float acc[C::TT][C::NACC];
 #pragma unroll
       for (int tt = 0; tt < C::TT; ++tt)

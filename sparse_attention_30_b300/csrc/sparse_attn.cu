@@ -146,7 +146,7 @@ __device__ __forceinline__ void gather_rows(const AttnArgs& a, int t, const int3
 // land), so producers never wait for their own copies and move straight on to the next stage.
 // The consumer issues fence.proxy.async after the barrier before the tensor core reads the stage.
 template <int NBLK>
-__device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const int32_t* idx_row, int n_tiles,
+__device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const int32_t* idx_row, int tile0, int n_tiles,
                                               uint32_t ring, int stage_bytes, int stages,
                                               uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
   const int pw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
@@ -160,8 +160,8 @@ __device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const in
   for (int i = 0; i < n_tiles; ++i) {
     const int st = i % stages;
     if (!warp_wait(baddr(empty[st]), ((i / stages) & 1) ^ 1, abort_flag, a)) break;
-    gather_rows<NBLK>(a, t, idx_row, i, ring + st * stage_bytes, pw, lane, fallback_row < 0 ? 0 : fallback_row,
-                      &range_err);
+    gather_rows<NBLK>(a, t, idx_row, tile0 + i, ring + st * stage_bytes, pw, lane,
+                      fallback_row < 0 ? 0 : fallback_row, &range_err);
     ptx::cp_async_arrive_noinc(baddr(full[st]));
   }
   ptx::cp_async_wait<0>();  // nothing of this thread's may still be in flight when the CTA exits
@@ -175,10 +175,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
   __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag_s;
-  __shared__ int n_tiles_s;
+  __shared__ int n_tiles_s, tile0_s;
 
   const int rank = static_cast<int>(ptx::cluster_ctarank());
-  const int t = blockIdx.x >> 1;
+  const int cl = blockIdx.x >> 1;
+  const int t = cl / a.n_split, sp = cl % a.n_split;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &abort_flag_s;
   const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.k;
@@ -216,7 +217,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
       const int mid = (lo + hi) >> 1;
       if (idx_row[mid] >= 0) lo = mid + 1; else hi = mid;
     }
-    n_tiles_s = (lo + kKT - 1) / kKT;
+    // this cluster's share of the token's tiles
+    const int all_tiles = (lo + kKT - 1) / kKT;
+    const int per = (all_tiles + a.n_split - 1) / a.n_split;
+    tile0_s = sp * per;
+    n_tiles_s = max(0, min(per, all_tiles - sp * per));
     ptx::fence_mbar_init();
     if (rank == 1 && n_tiles_s > 0) {
       // arm the first use of every P slot and the final statistics for rank 0's bulk copies
@@ -233,7 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
   ptx::cluster_sync_all();  // both CTAs' barriers exist (and are armed) before any remote traffic
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const int n_tiles = n_tiles_s;
+  const int n_tiles = n_tiles_s, tile0 = tile0_s;
 
   if (rank == 0) {
     // ================================================================ score CTA
@@ -263,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
       }
     } else if (warp <= kProdWarps) {
-      producer_loop<9>(a, t, idx_row, n_tiles, sbase + kOffK, kKStageBytes, kKStages, bars.k_full, bars.k_empty,
+      producer_loop<9>(a, t, idx_row, tile0, n_tiles, sbase + kOffK, kKStageBytes, kKStages, bars.k_full, bars.k_empty,
                        abort_flag);
     } else if (warp < kCreditWarp) {
       // ------------------------------------------------------------ Q -> TMEM, then softmax
@@ -310,7 +315,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         uint32_t vm[2];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int slot = i * kKT + hh * 32 + lane;
+          const int slot = (tile0 + i) * kKT + hh * 32 + lane;
           const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
           vm[hh] = __ballot_sync(0xffffffffu, latent_row(a, t, sidx, &range_err) >= 0);
         }
@@ -385,9 +390,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         }
         if (h == 0) ptx::bulk_wait_read<0>();
       }
-      if (a.lse != nullptr && h < a.H)
+      if (a.n_split > 1) {
+        if (h < a.H) {
+          float* ml = a.part_ml + ((static_cast<int64_t>(t) * a.n_split + sp) * a.H + h) * 2;
+          ml[0] = (ok && n_tiles > 0) ? m_used : -INFINITY;
+          ml[1] = (ok && n_tiles > 0) ? l : 0.f;
+        }
+      } else if (a.lse != nullptr && h < a.H) {
         a.lse[static_cast<int64_t>(t) * a.H + h] =
             (ok && n_tiles > 0) ? (m_used + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      }
     }
   } else {
     // ================================================================ value CTA
@@ -421,7 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
       }
     } else if (warp <= kProdWarps) {
-      producer_loop<8>(a, t, idx_row, n_tiles, sbase + kOffV, kVStageBytes, kVStages, bars.v_full, bars.v_empty,
+      producer_loop<8>(a, t, idx_row, tile0, n_tiles, sbase + kOffV, kVStageBytes, kVStages, bars.v_full, bars.v_empty,
                        abort_flag);
     } else if (warp < kCreditWarp) {
       // ------------------------------------------------------------ rescale, then epilogue
@@ -470,12 +482,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
       ptx::tc_fence_after();
       const bool has_rows = ok && n_tiles > 0;
       uint16_t* orow = a.out + (static_cast<int64_t>(t) * a.H + h) * kDV;
+      float* prow = a.part_o + ((static_cast<int64_t>(t) * a.n_split + sp) * a.H + h) * kDV;
 #pragma unroll 1
       for (int c = 0; c < 16; ++c) {
         uint32_t o[32];
         ptx::tmem_ld32(tmem + lane_base + c * 32, o);
         ptx::tmem_wait_ld();
-        if (h < a.H) {
+        if (a.n_split > 1) {
+          if (h < a.H) {
+            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = has_rows ? make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
+                                              __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        } else if (h < a.H) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
@@ -508,13 +530,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
   }
 }
 
+// Merges the key-split partial results of one (token, head) row: with per-split running max m_s
+// (log2 domain), sum l_s and normalised output O_s, the row's softmax weights over the union of the
+// splits give O = sum_s l_s 2^(m_s - m) O_s / sum_s l_s 2^(m_s - m), m = max_s m_s.
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
+  const int t = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int64_t base = static_cast<int64_t>(t) * a.n_split * a.H + h;
+  float m = -INFINITY;
+  for (int s = 0; s < a.n_split; ++s) m = fmaxf(m, a.part_ml[(base + static_cast<int64_t>(s) * a.H) * 2]);
+  float wsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < a.n_split; ++s) {
+    const int64_t r = base + static_cast<int64_t>(s) * a.H;
+    const float ms = a.part_ml[r * 2], ls = a.part_ml[r * 2 + 1];
+    const float wt = (ls > 0.f && m > -INFINITY) ? ls * fast_exp2(ms - m) : 0.f;
+    const float4 o = reinterpret_cast<const float4*>(a.part_o + r * kDV)[threadIdx.x];
+    acc.x += wt * o.x; acc.y += wt * o.y; acc.z += wt * o.z; acc.w += wt * o.w;
+    wsum += wt;
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint2 pk;
+  pk.x = pack_bf16(acc.x * inv, acc.y * inv);
+  pk.y = pack_bf16(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(t) * a.H + h) * kDV)[threadIdx.x] = pk;
+  if (threadIdx.x == 0 && a.lse != nullptr)
+    a.lse[static_cast<int64_t>(t) * a.H + h] = wsum > 0.f ? (m + __log2f(wsum)) * 0.69314718055994530942f : -INFINITY;
+}
+
 }  // namespace
 
-cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
-  if (a.T <= 0) return cudaSuccess;
+cudaError_t launch_sparse_attn(const AttnArgs& a0, cudaStream_t stream) {
+  if (a0.T <= 0) return cudaSuccess;
+  AttnArgs a = a0;
+  if (a.n_split < 1 || a.part_o == nullptr || a.part_ml == nullptr) a.n_split = 1;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<dim3(2 * a.T), kThreads, kSmem, stream>>>(a);
+  sparse_attn_kernel<<<dim3(2 * a.T * a.n_split), kThreads, kSmem, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.n_split == 1) return e;
+  return launch_attn_combine(a, stream);
+}
+
+cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream) {
+  attn_combine_kernel<<<a.T * a.H, kDV / 4, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

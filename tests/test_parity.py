@@ -222,6 +222,28 @@ def test_attention_ragged_selection_and_range_errors(dsa):
     _check_attention(out2.float().cpu().numpy()[0], None, o_ref, None, "range row")
 
 
+@pytest.mark.parametrize("n_split", [2, 3, 8])
+def test_attention_key_split_matches_oracle(dsa, n_split):
+    g = torch.Generator().manual_seed(21 + n_split)
+    T, H, S, k = 6, 128, 5000, 2048
+    q = torch.randn(T, H, 576, generator=g).to(torch.bfloat16)
+    kv = torch.randn(S, 576, generator=g).to(torch.bfloat16)
+    idx = torch.full((T, k), -1, dtype=torch.int32)
+    counts = [2048, 2000, 700, 65, 1, 0]                     # shares of 0 or partial tiles included
+    for t, c in enumerate(counts):
+        idx[t, :c] = torch.randperm(S, generator=g)[:c].to(torch.int32)
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    out, _ = dsa.sparse_attn_split(q.cuda(), kv.cuda(), idx.cuda(), 0.05, n_split, lse=lse)
+    assert dsa.device_status() == 0
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    for t, c in enumerate(counts):
+        if c == 0:
+            assert np.all(out[t] == 0) and np.all(np.isneginf(lse[t]))
+            continue
+        o_ref, l_ref = oracle.attention_row(q[t], kv[idx[t, :c].long()], 0.05)
+        _check_attention(out[t], lse[t], o_ref, l_ref, f"split {n_split} row {t}")
+
+
 # ----------------------------------------------------------------------------- fused forward
 
 
@@ -267,6 +289,22 @@ def test_forward_decode_full_config(dsa, cid):
     idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
     for b in range(cfg.B):
         _check_row(hinp, b, cfg.k, cfg.scale, idx[b], out[b], lse[b], decode=True, where=f"cfg{cid}")
+
+
+def test_forward_decode_small_batch_splits_keys(dsa):
+    # two sequences: the driver spreads each sequence's selected keys over four clusters and merges
+    cfg = synth.config(5, B=2, ctx_lo=3000, ctx_hi=9000, seed=9)
+    d = synth.decode_inputs(cfg, device="cuda")
+    max_len = int(d["seq_lens"].max())
+    idx = torch.empty((cfg.B, cfg.k), dtype=torch.int32, device="cuda")
+    lse = torch.empty((cfg.B, cfg.H), dtype=torch.float32, device="cuda")
+    f = dsa.Forward.decode(d, cfg.k, cfg.scale, max_len, lse=lse, idx=idx)
+    f()
+    assert dsa.device_status() == 0
+    hinp = _host(d)
+    idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
+    for b in range(cfg.B):
+        _check_row(hinp, b, cfg.k, cfg.scale, idx[b], out[b], lse[b], decode=True, where="split")
 
 
 def test_forward_prefill_config4_full_size_sampled_rows(dsa):
