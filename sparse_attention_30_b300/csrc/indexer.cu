@@ -31,7 +31,7 @@ struct IdxCfg {
   static constexpr int NCOL = PAGED ? HI : 256;
   static constexpr int TT = NCOL / HI;
   static constexpr int NACC = (TT >= 32) ? 1 : ((32 / TT) < 4 ? (32 / TT) : 4);
-  static constexpr int STAGES = PAGED ? 8 : 6;
+  static constexpr int STAGES = 6;  // decode: small enough for two CTAs per SM
   static constexpr int Q_BYTES = NCOL * kRowBytes;
   static constexpr int TMEM_COLS = pow2_cols(2 * NCOL);
   static constexpr int OFF_Q = 0;
@@ -53,7 +53,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 }
 
 template <int HI, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, PAGED ? 2 : 1)
     indexer_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const IndexerArgs a) {
   using C = IdxCfg<HI, PAGED>;
@@ -307,8 +307,8 @@ cudaError_t launch_t(const CUtensorMap& qm, const CUtensorMap& km, int max_keys,
   const int n_key_tiles = (max_keys + kTileKeys - 1) / kTileKeys;
   const int gx = PAGED ? a.rows : (a.rows + C::TT - 1) / C::TT;
   if (PAGED) {
-    // spread a batch's keys over about four CTAs per SM
-    const int64_t want = 4 * 148;
+    // spread a batch's keys over about eight CTAs per SM (two resident at a time)
+    const int64_t want = 8 * 148;
     int64_t tpc = (static_cast<int64_t>(gx) * n_key_tiles + want - 1) / want;
     a.tiles_per_cta = static_cast<int>(tpc < 1 ? 1 : tpc);
   } else {
