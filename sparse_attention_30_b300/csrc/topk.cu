@@ -1,19 +1,21 @@
 // Fine-grained token selection (freezhihu.org/question/1978819912970555965, §2.1.2):
 // for each query row keep the k positions with the largest indexer scores.
 //
-// One CTA per row runs an exact radix select on order-preserving 32-bit keys:
-//   pass 1  (reads the row)   histogram of the top 12 key bits in shared memory;
-//                             a block suffix-scan (warp shuffles) finds the bin B that
-//                             holds the k-th largest key;
-//   pass 2  (reads the row)   positions in bins above B go straight to the output; keys
-//                             in bin B are kept as (key, position) candidates in shared
-//                             memory (if more than kCandCap, the next levels re-read the
-//                             row from global memory instead);
-//   levels 2, 3               12-bit and 8-bit histograms of the candidates pin the exact
-//                             32-bit threshold key and how many keys equal to it to take;
-//   final                     candidates above the threshold, then the needed number of
-//                             equal ones, are appended to the output.
-// Output slots are filled in no particular order; rows with n <= k select everything.
+// One CTA per row; scores become order-preserving 32-bit keys and the selection is exact.
+//   n <= k         every position is selected.
+//   n <= kCandCap  the row is loaded into shared memory once and selected there.
+//   otherwise      (sample and filter) a strided sample of kSample keys gives a lower bound
+//                  tau that the k-th largest key clears with overwhelming probability: the
+//                  sample's rank-r key, r = the expected sample rank of the k-th largest key
+//                  + 4 standard deviations + 2.  One pass over the row compacts the keys >= tau
+//                  into shared memory; when between k and kCandCap of them were found, the
+//                  exact selection runs on those.  Otherwise (a sample that missed, or heavy
+//                  ties at tau) the row falls back to a radix select that re-reads it.
+// The selection in shared memory is a three-level radix select (12 + 12 + 8 key bits); each
+// level finds its bin with a block suffix scan built from warp shuffles.  Output slots are
+// filled in no particular order.
+#include <math.h>
+
 #include "dsa_internal.h"
 
 namespace dsa {
@@ -23,6 +25,9 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;
 constexpr int kCandCap = 6144;
+constexpr int kSample = 4096;  // held in cand_key until the filter pass starts
+constexpr int kUnroll = 8;     // float4 loads in flight per thread in the filter pass
+static_assert(kSample <= kCandCap, "the sample is staged in the candidate buffer");
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x);
@@ -73,18 +78,81 @@ __device__ void select_bin(TopkSmem& s, int nbins, uint32_t kk) {
   __syncthreads();
 }
 
-// Visits the keys of bin `top` (top 12 bits) either from the candidate buffer or, if it
-// overflowed, by re-reading the row.  f(key, pos) is called for each.
-template <class F>
-__device__ __forceinline__ void for_each_candidate(const TopkSmem& s, bool in_smem, uint32_t ncand,
-                                                   const float* row, int n, uint32_t top, F&& f) {
-  if (in_smem) {
-    for (uint32_t i = threadIdx.x; i < ncand; i += kThreads) f(s.cand_key[i], s.cand_pos[i]);
+// Three-level radix select over keys visited by `each(f)` (f(key) per key): returns the key
+// thr of the rank-th largest and how many keys equal to thr belong to the top `rank`.
+// With kLevels == 2 the last 8 key bits are left open: thr is the lowest key of the 24-bit prefix
+// that holds the rank-th largest key (a lower bound of it) and n_equal is not set.
+template <int kLevels = 3, class Each>
+__device__ void radix_threshold(TopkSmem& s, uint32_t rank, Each&& each, uint32_t* thr, uint32_t* n_equal) {
+  const int tid = threadIdx.x;
+  for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
+  __syncthreads();
+  each([&](uint32_t key) { atomicAdd(&s.hist[key >> 20], 1u); });
+  __syncthreads();
+  select_bin(s, kBins, rank);
+  const uint32_t top = s.sel_bin;
+  uint32_t need = rank - s.sel_above;
+  __syncthreads();
+  for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
+  __syncthreads();
+  each([&](uint32_t key) {
+    if ((key >> 20) == top) atomicAdd(&s.hist[(key >> 8) & 0xFFFu], 1u);
+  });
+  __syncthreads();
+  select_bin(s, kBins, need);
+  const uint32_t pre24 = (top << 12) | s.sel_bin;
+  need -= s.sel_above;
+  __syncthreads();
+  if constexpr (kLevels == 2) {
+    *thr = pre24 << 8;
   } else {
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      const uint32_t key = order_key(row[i]);
-      if ((key >> 20) == top) f(key, i);
+    for (int b = tid; b < 256; b += kThreads) s.hist[b] = 0;
+    __syncthreads();
+    each([&](uint32_t key) {
+      if ((key >> 8) == pre24) atomicAdd(&s.hist[key & 0xFFu], 1u);
+    });
+    __syncthreads();
+    select_bin(s, 256, need);
+    *thr = (pre24 << 8) | s.sel_bin;
+    *n_equal = need - s.sel_above;
+    __syncthreads();
+  }
+}
+
+// Appends, warp-aggregated, the positions whose predicate holds to out[] through counter *n.
+__device__ __forceinline__ void append(uint32_t* n, int32_t* out, uint32_t cap, bool take, int pos,
+                                       uint32_t key, uint32_t* keys) {
+  const uint32_t active = __activemask();
+  const uint32_t m = __ballot_sync(active, take);
+  if (!m) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(active) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(n, static_cast<uint32_t>(__popc(m)));
+  base = __shfl_sync(active, base, leader);
+  if (take) {
+    const uint32_t c = base + __popc(m & ((1u << lane) - 1u));
+    if (c < cap) {
+      out[c] = pos;
+      if (keys) keys[c] = key;
     }
+  }
+}
+
+// Emits the top k of the `count` candidates in shared memory (k <= count).
+__device__ void select_from_candidates(TopkSmem& s, uint32_t count, uint32_t k, int32_t* out) {
+  uint32_t thr, n_equal;
+  radix_threshold(
+      s, k,
+      [&](auto&& f) {
+        for (uint32_t i = threadIdx.x; i < count; i += kThreads) f(s.cand_key[i]);
+      },
+      &thr, &n_equal);
+  for (uint32_t i = threadIdx.x; i < count; i += kThreads) {
+    const uint32_t key = s.cand_key[i];
+    bool take = key > thr;
+    if (key == thr) take = atomicAdd(&s.n_eq, 1u) < n_equal;
+    append(&s.n_out, out, k, take, s.cand_pos[i], 0, nullptr);
   }
 }
 
@@ -98,91 +166,118 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   if (n64 > a.ld) n64 = a.ld;
   if (n64 < 0) n64 = 0;
   const int n = static_cast<int>(n64);
-  const int k = a.k;
-  int32_t* out = a.idx + static_cast<int64_t>(t) * k;
-  const float* row = a.scores + static_cast<int64_t>(t) * a.ld;
+  const uint32_t k = static_cast<uint32_t>(a.k);
+  int32_t* out = a.idx + static_cast<int64_t>(t) * a.k;
+  const float* row = a.scores + static_cast<int64_t>(t) * a.ld;  // 16-byte aligned rows
 
-  if (n <= k) {
-    for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
+  if (static_cast<uint32_t>(n) <= k) {
+    for (int i = tid; i < a.k; i += kThreads) out[i] = i < n ? i : -1;
+    return;
+  }
+  if (tid == 0) { s.n_out = 0; s.n_cand = 0; s.n_eq = 0; }
+
+  if (n <= kCandCap) {
+    // the whole row fits: one read, exact selection in shared memory
+    for (int i = tid; i < n; i += kThreads) {
+      s.cand_key[i] = order_key(row[i]);
+      s.cand_pos[i] = i;
+    }
+    __syncthreads();
+    select_from_candidates(s, n, k, out);
     return;
   }
 
-  for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
-  if (tid == 0) { s.n_out = 0; s.n_cand = 0; s.n_eq = 0; }
+  // ---- sample: kSample keys at evenly spread positions; tau = the sample's rank-r key
+  {
+    constexpr int kPer = kSample / kThreads;
+    float v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) v[u] = row[static_cast<int64_t>(tid + u * kThreads) * n / kSample];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) s.cand_key[tid + u * kThreads] = order_key(v[u]);
+  }
   __syncthreads();
+  const float mu = static_cast<float>(k) * kSample / n;  // expected sample keys >= the k-th largest
+  uint32_t r = static_cast<uint32_t>(mu + 4.f * sqrtf(mu) + 2.f);
+  if (r > kSample) r = kSample;
+  uint32_t tau, unused;
+  radix_threshold<2>(
+      s, r,
+      [&](auto&& f) {
+        for (int i = tid; i < kSample; i += kThreads) f(s.cand_key[i]);
+      },
+      &tau, &unused);
+  // keys >= tau as a float bound: {x >= tau_f} is a prefix of the key order for non-NaN x
+  // (it takes both zeros or neither), so it holds the row's top k whenever it has k members
+  const float tau_f = __uint_as_float((tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau);
 
-  // ---- pass 1: top-12-bit histogram (rows are 16-byte aligned: ld % 4 == 0)
+  // ---- filter: compact the positions with x >= tau_f (counting those beyond capacity)
   const int n4 = n >> 2;
   const float4* row4 = reinterpret_cast<const float4*>(row);
-  for (int i = tid; i < n4; i += kThreads) {
-    const float4 v = row4[i];
-    atomicAdd(&s.hist[order_key(v.x) >> 20], 1u);
-    atomicAdd(&s.hist[order_key(v.y) >> 20], 1u);
-    atomicAdd(&s.hist[order_key(v.z) >> 20], 1u);
-    atomicAdd(&s.hist[order_key(v.w) >> 20], 1u);
-  }
-  for (int i = (n4 << 2) + tid; i < n; i += kThreads) atomicAdd(&s.hist[order_key(row[i]) >> 20], 1u);
-  __syncthreads();
-  select_bin(s, kBins, static_cast<uint32_t>(k));
-  const uint32_t top = s.sel_bin;
-  uint32_t need = static_cast<uint32_t>(k) - s.sel_above;  // keys still to take from bin `top`
-  const uint32_t ncand = s.hist[top];
-  const bool in_smem = ncand <= static_cast<uint32_t>(kCandCap);
-  __syncthreads();
-
-  // ---- pass 2: emit bins above `top`, collect bin `top`
-  auto visit = [&](uint32_t key, int pos) {
-    const uint32_t b = key >> 20;
-    if (b > top) {
-      out[atomicAdd(&s.n_out, 1u)] = pos;
-    } else if (b == top && in_smem) {
-      const uint32_t c = atomicAdd(&s.n_cand, 1u);
-      s.cand_key[c] = key;
-      s.cand_pos[c] = pos;
+  const int lane = tid & 31;
+  for (int b = 0; b < n4; b += kThreads * kUnroll) {  // block-uniform trip count
+    const int i0 = b + tid;
+    float4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u * kThreads;
+      v[u] = i < n4 ? __ldcs(row4 + i) : make_float4(NAN, NAN, NAN, NAN);  // NaN never passes
     }
-  };
-  for (int i = tid; i < n4; i += kThreads) {
-    const float4 v = row4[i];
-    visit(order_key(v.x), 4 * i);
-    visit(order_key(v.y), 4 * i + 1);
-    visit(order_key(v.z), 4 * i + 2);
-    visit(order_key(v.w), 4 * i + 3);
-  }
-  for (int i = (n4 << 2) + tid; i < n; i += kThreads) visit(order_key(row[i]), i);
-  __syncthreads();
-
-  // ---- level 2: bits 19..8 of the keys in bin `top`
-  for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
-  __syncthreads();
-  for_each_candidate(s, in_smem, ncand, row, n, top,
-                     [&](uint32_t key, int) { atomicAdd(&s.hist[(key >> 8) & 0xFFFu], 1u); });
-  __syncthreads();
-  select_bin(s, kBins, need);
-  const uint32_t mid = s.sel_bin;
-  need -= s.sel_above;
-  __syncthreads();
-
-  // ---- level 3: bits 7..0 of the keys with prefix (top, mid)
-  for (int b = tid; b < 256; b += kThreads) s.hist[b] = 0;
-  __syncthreads();
-  const uint32_t pre24 = (top << 12) | mid;
-  for_each_candidate(s, in_smem, ncand, row, n, top, [&](uint32_t key, int) {
-    if ((key >> 8) == pre24) atomicAdd(&s.hist[key & 0xFFu], 1u);
-  });
-  __syncthreads();
-  select_bin(s, 256, need);
-  const uint32_t thr = (pre24 << 8) | s.sel_bin;
-  const uint32_t n_equal = need - s.sel_above;  // keys equal to thr to take
-  __syncthreads();
-
-  // ---- final: candidates above the threshold, then n_equal of those equal to it
-  for_each_candidate(s, in_smem, ncand, row, n, top, [&](uint32_t key, int pos) {
-    if (key > thr) {
-      out[atomicAdd(&s.n_out, 1u)] = pos;
-    } else if (key == thr) {
-      if (atomicAdd(&s.n_eq, 1u) < n_equal) out[atomicAdd(&s.n_out, 1u)] = pos;
+    uint32_t mask = 0;  // bit 4u + c: element c of v[u]
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      mask |= (v[u].x >= tau_f ? 1u : 0u) << (4 * u);
+      mask |= (v[u].y >= tau_f ? 2u : 0u) << (4 * u);
+      mask |= (v[u].z >= tau_f ? 4u : 0u) << (4 * u);
+      mask |= (v[u].w >= tau_f ? 8u : 0u) << (4 * u);
     }
-  });
+    if (!__any_sync(0xffffffffu, mask != 0)) continue;
+    const uint32_t cnt = __popc(mask);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    uint32_t base = 0;
+    if (lane == 31) base = atomicAdd(&s.n_cand, incl);
+    base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+    while (mask) {
+      const int bit = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int pos = 4 * (i0 + (bit >> 2) * kThreads) + (bit & 3);
+      if (base < static_cast<uint32_t>(kCandCap)) {
+        s.cand_key[base] = order_key(row[pos]);  // an L1 hit
+        s.cand_pos[base] = pos;
+      }
+      ++base;
+    }
+  }
+  for (int i = (n4 << 2) + tid; i < n; i += kThreads) {
+    const float x = row[i];
+    append(&s.n_cand, s.cand_pos, kCandCap, x >= tau_f, i, order_key(x), s.cand_key);
+  }
+  __syncthreads();
+  const uint32_t found = s.n_cand;
+  if (found >= k && found <= static_cast<uint32_t>(kCandCap)) {
+    select_from_candidates(s, found, k, out);
+    return;
+  }
+
+  // ---- fallback: radix select over the whole row, re-read from global memory
+  uint32_t thr, n_equal;
+  radix_threshold(
+      s, k,
+      [&](auto&& f) {
+        for (int i = tid; i < n; i += kThreads) f(order_key(row[i]));
+      },
+      &thr, &n_equal);
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t key = order_key(row[i]);
+    bool take = key > thr;
+    if (key == thr) take = atomicAdd(&s.n_eq, 1u) < n_equal;
+    append(&s.n_out, out, k, take, i, 0, nullptr);
+  }
 }
 
 }  // namespace

@@ -136,8 +136,9 @@ def _topk_valid(vals, sel, k):
     assert np.isin(strict, sel).all()
 
 
-@pytest.mark.parametrize("dist", ["normal", "ties", "const", "lognormal", "negative", "tiny_range"])
-@pytest.mark.parametrize("n,k", [(100, 64), (2049, 2048), (4097, 2048), (131072, 2048), (70000, 64), (3000, 1)])
+@pytest.mark.parametrize("dist", ["normal", "ties", "const", "lognormal", "negative", "tiny_range", "spikes"])
+@pytest.mark.parametrize("n,k", [(100, 64), (2049, 2048), (4097, 2048), (6144, 2048), (6145, 2048),
+                                 (131072, 2048), (70000, 64), (3000, 1)])
 def test_topk_exact_on_fixed_scores(dsa, dist, n, k):
     rng = np.random.default_rng(n * 7 + k)
     T = 3
@@ -151,6 +152,11 @@ def test_topk_exact_on_fixed_scores(dsa, dist, n, k):
         v = rng.lognormal(0, 2.0, (T, n))
     elif dist == "negative":
         v = -np.abs(rng.standard_normal((T, n))) * 1e3
+    elif dist == "spikes":
+        # large values on an evenly strided grid of 4096 positions, small ones elsewhere:
+        # a strided sample of the row sees only the spikes
+        v = rng.random((T, n))
+        v[:, (np.arange(4096) * n) // 4096] += 100.0
     else:
         v = 1.0 + rng.integers(0, 50, (T, n)) * 2.0 ** -23
     v = v.astype(np.float32)
