@@ -53,8 +53,8 @@ __global__ void wait_timeout_kernel(int* status, uint64_t limit_ns) {
 
 }  // namespace
 
-bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                       uint32_t box_rows) {
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_encode) {
@@ -68,12 +68,17 @@ bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint6
     }
   }
   const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner};
+  const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t elem[2] = {1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, elem,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                       uint32_t box_rows) {
+  return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, rows, inner, box_inner, box_rows);
 }
 
 cudaError_t launch_wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {

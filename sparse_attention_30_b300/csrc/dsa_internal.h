@@ -12,6 +12,11 @@ namespace dsa {
 // Bounded waits give up after this long (about one second).
 constexpr uint64_t kWaitLimitNs = 1ull << 30;
 
+// 2-D tensor map over a row-major matrix [rows, inner] with the given row pitch, 128-byte swizzle,
+// box [box_inner, box_rows]; false if the driver rejects it.
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+
 // ---------------------------------------------------------------- indexer
 
 struct IndexerArgs {

@@ -184,6 +184,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 2-D tiled TMA store of a shared-memory box (bulk async group of the issuing thread).  The box
+// must be written and made visible to the async proxy (fence.proxy.async) before the store.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+
 // 16-byte cp.async (L2 only); with valid == false the 16 destination bytes are zero-filled
 // and nothing is read.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {

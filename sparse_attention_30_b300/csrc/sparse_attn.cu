@@ -48,6 +48,8 @@ constexpr int kSlotFlag = kSlotFac + 128 * 4;
 constexpr int kSlotBytes = kSlotFlag + 16;     // bytes moved per tile
 constexpr int kSlotStride = 17408;
 constexpr int kStatsBytes = 1024;              // l[128], m[128]
+constexpr int kQBoxBytes = 128 * 128;          // Q / O staging box: 128 rows x 128 bytes, 128B-swizzled
+constexpr int kQBytes = 9 * kQBoxBytes;        // Q [128 x 576] bf16
 // rank 0 layout
 constexpr int kOffK = 0;
 constexpr int kOffStage = kOffK + kKStages * kKStageBytes;
@@ -62,6 +64,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 288;                // rank 0: Q in columns 0..287, S buffers after it
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 static_assert(kColS + kSBufs * kKT <= kTmemCols, "rank 0 TMEM budget");
+static_assert(kQBytes <= kKStages * kKStageBytes, "Q is staged in rank 0's K ring");
+static_assert(8 * kQBoxBytes <= kVStages * kVStageBytes, "O is staged in rank 1's V ring, 8 boxes at a time");
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -90,7 +94,7 @@ __device__ __forceinline__ int64_t latent_row(const AttnArgs& a, int t, int32_t 
 
 struct Bars {
   // rank 0
-  uint64_t k_full[kKStages], k_empty[kKStages], s_full[kSBufs], s_empty[kSBufs], q_ready, p_empty[kSlots];
+  uint64_t k_full[kKStages], k_empty[kKStages], s_full[kSBufs], s_empty[kSBufs], q_full, q_ready, p_empty[kSlots];
   // rank 1
   uint64_t v_full[kVStages], v_empty[kVStages], p_full[kSlots], ready[kSlots], slot_free[kSlots], stats_full;
   uint64_t mma_done;
@@ -148,10 +152,13 @@ __device__ __forceinline__ void gather_rows(const AttnArgs& a, int t, const int3
 template <int NBLK>
 __device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const int32_t* idx_row, int tile0, int n_tiles,
                                               uint32_t ring, int stage_bytes, int stages,
-                                              uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
+                                              uint64_t* full, uint64_t* empty, volatile int* abort_flag,
+                                              uint64_t* start) {
   const int pw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
   bool range_err = false;
   if (n_tiles <= 0) return;
+  // rank 0's ring holds Q until it has been moved into tensor memory
+  if (start != nullptr && !warp_wait(baddr(*start), 0, abort_flag, a)) return;
   // the first slot is valid whenever there is a tile (valid slots come first)
   const int64_t fallback_row = latent_row(a, t, __ldg(idx_row), &range_err);
   if (fallback_row < 0) {  // first position out of range: nothing safe to substitute
@@ -168,14 +175,16 @@ __device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const in
   if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap omap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag_s;
-  __shared__ int n_tiles_s, tile0_s;
+  __shared__ int first_empty_s;
 
   const int rank = static_cast<int>(ptx::cluster_ctarank());
   const int cl = blockIdx.x >> 1;
@@ -184,6 +193,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
   volatile int* abort_flag = &abort_flag_s;
   const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.k;
   const uint32_t sbase = ptx::smem_addr(smem);
+
+  // valid slots come first: the token's tile count follows from its first empty slot, found by
+  // every thread scanning a strided share of the row (the loads overlap the setup below)
+  int first_empty = a.k;
+#pragma unroll 4
+  for (int i = tid; i < a.k; i += kThreads)
+    if (__ldg(idx_row + i) < 0) first_empty = min(first_empty, i);
 
   if (tid == 0) {
     if (rank == 0) {
@@ -195,6 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         ptx::mbar_init(baddr(bars.s_full[b]), 1);
         ptx::mbar_init(baddr(bars.s_empty[b]), 128);
       }
+      ptx::mbar_init(baddr(bars.q_full), 1);
       ptx::mbar_init(baddr(bars.q_ready), 128);
       for (int s = 0; s < kSlots; ++s) ptx::mbar_init(baddr(bars.p_empty[s]), 1);
     } else {
@@ -211,34 +228,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
     }
     ptx::mbar_init(baddr(bars.mma_done), 1);
     abort_flag_s = 0;
-    // valid slots come first: the number of tiles follows from the first empty slot
-    int lo = 0, hi = a.k;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (idx_row[mid] >= 0) lo = mid + 1; else hi = mid;
-    }
-    // this cluster's share of the token's tiles
-    const int all_tiles = (lo + kKT - 1) / kKT;
-    const int per = (all_tiles + a.n_split - 1) / a.n_split;
-    tile0_s = sp * per;
-    n_tiles_s = max(0, min(per, all_tiles - sp * per));
+    first_empty_s = a.k;
     ptx::fence_mbar_init();
-    if (rank == 1 && n_tiles_s > 0) {
-      // arm the first use of every P slot and the final statistics for rank 0's bulk copies
-      for (int s = 0; s < kSlots; ++s) ptx::mbar_arrive_expect_tx(baddr(bars.p_full[s]), kSlotBytes);
-      ptx::mbar_arrive_expect_tx(baddr(bars.stats_full), kStatsBytes);
-    }
   }
   if (warp == 0) {
     ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
+  }
+  __syncthreads();
+  if (first_empty < a.k) atomicMin(&first_empty_s, first_empty);
+  __syncthreads();
+  // this cluster's share of the token's tiles
+  const int all_tiles = (first_empty_s + kKT - 1) / kKT;
+  const int per = (all_tiles + a.n_split - 1) / a.n_split;
+  const int tile0 = sp * per;
+  const int n_tiles = max(0, min(per, all_tiles - sp * per));
+  if (tid == 0 && n_tiles > 0) {
+    if (rank == 1) {
+      // arm the first use of every P slot and the final statistics for rank 0's bulk copies
+      for (int s = 0; s < kSlots; ++s) ptx::mbar_arrive_expect_tx(baddr(bars.p_full[s]), kSlotBytes);
+      ptx::mbar_arrive_expect_tx(baddr(bars.stats_full), kStatsBytes);
+    } else {
+      // Q [128 x 576] of the token -> the K ring, as nine 128B-swizzled [128 x 64] boxes (rows past
+      // the tensor read as zero; rows of the next token, when H < 128, are never used)
+      ptx::mbar_arrive_expect_tx(baddr(bars.q_full), kQBytes);
+#pragma unroll 1
+      for (int b = 0; b < 9; ++b)
+        ptx::tma_load_2d(sbase + kOffK + b * kQBoxBytes, &qmap, baddr(bars.q_full), b * 64, t * a.H);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::cluster_sync_all();  // both CTAs' barriers exist (and are armed) before any remote traffic
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const int n_tiles = n_tiles_s, tile0 = tile0_s;
 
   if (rank == 0) {
     // ================================================================ score CTA
@@ -269,22 +292,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
       }
     } else if (warp <= kProdWarps) {
       producer_loop<9>(a, t, idx_row, tile0, n_tiles, sbase + kOffK, kKStageBytes, kKStages, bars.k_full, bars.k_empty,
-                       abort_flag);
+                       abort_flag, &bars.q_ready);
     } else if (warp < kCreditWarp) {
       // ------------------------------------------------------------ Q -> TMEM, then softmax
       const int h = (warp & 3) * 32 + lane;
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      {
-        const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(t) * a.H + h) * kDL);
+      if (n_tiles > 0) {
+        // row h of box b sits at b * 16 KB + h * 128 B with its 16-byte chunks XOR-swizzled by h & 7
+        const bool got = warp_wait(baddr(bars.q_full), 0, abort_flag, a);
+        const uint8_t* qs = smem + kOffK + h * 128;
 #pragma unroll 1
-        for (int c = 0; c < 9; ++c) {
+        for (int b = 0; b < 9; ++b) {
           uint32_t v[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 x = h < a.H ? __ldg(qsrc + c * 8 + j) : make_uint4(0, 0, 0, 0);
-            v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+          for (int c = 0; c < 8; ++c) {
+            const uint4 x = (got && h < a.H) ? *reinterpret_cast<const uint4*>(qs + b * kQBoxBytes + ((c ^ (h & 7)) << 4))
+                                             : make_uint4(0, 0, 0, 0);
+            v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
           }
-          ptx::tmem_st32(tmem + lane_base + c * 32, v);
+          ptx::tmem_st32(tmem + lane_base + b * 32, v);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -434,7 +460,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
       }
     } else if (warp <= kProdWarps) {
       producer_loop<8>(a, t, idx_row, tile0, n_tiles, sbase + kOffV, kVStageBytes, kVStages, bars.v_full, bars.v_empty,
-                       abort_flag);
+                       abort_flag, nullptr);
     } else if (warp < kCreditWarp) {
       // ------------------------------------------------------------ rescale, then epilogue
       const int h = (warp & 3) * 32 + lane;
@@ -470,7 +496,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
         ptx::tc_fence_before();
         ptx::mbar_arrive(baddr(bars.ready[ps]));
       }
-      // ---- epilogue: O / l -> bf16
+      // ---- epilogue: O / l, staged as 128B-swizzled [H x 128 B] boxes in the (drained) V ring and
+      // written by TMA stores: bf16 out (8 boxes of 64 columns) or, with a key split, the fp32
+      // partial (16 boxes of 32 columns, in two rounds of 8)
       float inv_l = 0.f;
       if (ok && n_tiles > 0) {
         const int j = n_tiles - 1;
@@ -481,32 +509,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sparse_
       }
       ptx::tc_fence_after();
       const bool has_rows = ok && n_tiles > 0;
-      uint16_t* orow = a.out + (static_cast<int64_t>(t) * a.H + h) * kDV;
-      float* prow = a.part_o + ((static_cast<int64_t>(t) * a.n_split + sp) * a.H + h) * kDV;
+      const bool split = a.n_split > 1;
+      const int out_row0 = split ? (t * a.n_split + sp) * a.H : t * a.H;
+      uint8_t* stage_row = smem + kOffV + h * 128;
 #pragma unroll 1
-      for (int c = 0; c < 16; ++c) {
-        uint32_t o[32];
-        ptx::tmem_ld32(tmem + lane_base + c * 32, o);
-        ptx::tmem_wait_ld();
-        if (a.n_split > 1) {
+      for (int round = 0; round < (split ? 2 : 1); ++round) {
+#pragma unroll 1
+        for (int cc = 0; cc < (split ? 8 : 16); ++cc) {
+          const int c = round * 8 + cc;  // 32-column block of O
+          uint32_t o[32];
+          ptx::tmem_ld32(tmem + lane_base + c * 32, o);
+          ptx::tmem_wait_ld();
           if (h < a.H) {
-            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+            if (split) {
+              uint8_t* box = stage_row + cc * kQBoxBytes;
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[e] = has_rows ? make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
-                                              __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int e = 0; e < 8; ++e)
+                *reinterpret_cast<float4*>(box + ((e ^ (h & 7)) << 4)) =
+                    has_rows ? make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
+                                           __uint_as_float(o[4 * e + 2]) * inv_l,
+                                           __uint_as_float(o[4 * e + 3]) * inv_l)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+              uint8_t* box = stage_row + (c >> 1) * kQBoxBytes;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int chunk = (c & 1) * 4 + e;
+                uint4 pk = make_uint4(0, 0, 0, 0);
+                if (has_rows) {
+                  pk.x = pack_bf16(__uint_as_float(o[8 * e]) * inv_l, __uint_as_float(o[8 * e + 1]) * inv_l);
+                  pk.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv_l, __uint_as_float(o[8 * e + 3]) * inv_l);
+                  pk.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv_l, __uint_as_float(o[8 * e + 5]) * inv_l);
+                  pk.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv_l, __uint_as_float(o[8 * e + 7]) * inv_l);
+                }
+                *reinterpret_cast<uint4*>(box + ((chunk ^ (h & 7)) << 4)) = pk;
+              }
+            }
           }
-        } else if (h < a.H) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = has_rows ? pack_bf16(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l)
-                             : 0u;
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
+        ptx::fence_proxy_async_smem();  // staged boxes (generic-proxy writes) -> TMA reads
+        ptx::named_sync(1, 128);
+        if (h == 0) {
+#pragma unroll 1
+          for (int b = 0; b < 8; ++b)
+            ptx::tma_store_2d(&omap, ptx::smem_addr(smem + kOffV + b * kQBoxBytes),
+                              split ? (round * 8 + b) * 32 : b * 64, out_row0);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read<0>();  // the staging boxes are free again (and before the CTA exits)
+        }
+        ptx::named_sync(1, 128);
       }
     } else if (lane == 0) {
       // ------------------------------------------------------------ slot credits back to rank 0
@@ -563,9 +614,20 @@ cudaError_t launch_sparse_attn(const AttnArgs& a0, cudaStream_t stream) {
   if (a0.T <= 0) return cudaSuccess;
   AttnArgs a = a0;
   if (a.n_split < 1 || a.part_o == nullptr || a.part_ml == nullptr) a.n_split = 1;
+  // Q viewed as [T*H, 576] bf16 (box 64 x 128); out as [T*H, 512] bf16 (box 64 x H) or the fp32
+  // partials as [T*n_split*H, 512] (box 32 x H): a box never covers another token's rows
+  CUtensorMap qmap, omap;
+  const uint64_t rows = static_cast<uint64_t>(a.T) * a.H;
+  if (!encode_tmap_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kDL, rows, kDL * 2, 64, 128))
+    return cudaErrorInvalidValue;
+  const bool ok = a.n_split > 1
+                      ? encode_tmap_2d(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.part_o, kDV, rows * a.n_split, kDV * 4,
+                                       32, a.H)
+                      : encode_tmap_2d(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out, kDV, rows, kDV * 2, 64, a.H);
+  if (!ok) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<dim3(2 * a.T * a.n_split), kThreads, kSmem, stream>>>(a);
+  sparse_attn_kernel<<<dim3(2 * a.T * a.n_split), kThreads, kSmem, stream>>>(a, qmap, omap);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_split == 1) return e;
   return launch_attn_combine(a, stream);
