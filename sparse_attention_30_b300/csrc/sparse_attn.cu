@@ -254,7 +254,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive_expect_tx(baddr(bars.q_full), kQBytes);
 #pragma unroll 1
       for (int b = 0; b < 9; ++b)
-        ptx::tma_load_2d(sbase + kOffK + b * kQBoxBytes, &qmap, baddr(bars.q_full), b * 64, t * a.H);
+        ptx::tma_load_2d_hint(sbase + kOffK + b * kQBoxBytes, &qmap, baddr(bars.q_full), b * 64, t * a.H,
+                              ptx::l2_evict_first_policy());  // Q and O stream through: keep L2 for latent rows
     }
   }
   ptx::tc_fence_before();
@@ -552,8 +553,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (h == 0) {
 #pragma unroll 1
           for (int b = 0; b < 8; ++b)
-            ptx::tma_store_2d(&omap, ptx::smem_addr(smem + kOffV + b * kQBoxBytes),
-                              split ? (round * 8 + b) * 32 : b * 64, out_row0);
+            ptx::tma_store_2d_hint(&omap, ptx::smem_addr(smem + kOffV + b * kQBoxBytes),
+                                   split ? (round * 8 + b) * 32 : b * 64, out_row0, ptx::l2_evict_first_policy());
           ptx::bulk_commit();
           ptx::bulk_wait_read<0>();  // the staging boxes are free again (and before the CTA exits)
         }
