@@ -176,8 +176,7 @@ __device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const in
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap,
-                       const __grid_constant__ CUtensorMap omap) {
+    sparse_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -430,6 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================================================================ value CTA
+    bool rescale_ok = true;
     if (warp == 0) {
       if (n_tiles > 0) {
         // ---- O += P V over two N = 256 halves, issued by the whole warp (one elected lane)
@@ -497,69 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(baddr(bars.ready[ps]));
       }
-      // ---- epilogue: O / l, staged as 128B-swizzled [H x 128 B] boxes in the (drained) V ring and
-      // written by TMA stores: bf16 out (8 boxes of 64 columns) or, with a key split, the fp32
-      // partial (16 boxes of 32 columns, in two rounds of 8)
-      float inv_l = 0.f;
-      if (ok && n_tiles > 0) {
-        const int j = n_tiles - 1;
-        ok = ptx::mbar_wait(baddr(bars.stats_full), 0, abort_flag, a.status, a.limit_ns) &&
-             ptx::mbar_wait(baddr(bars.slot_free[j % kSlots]), (j / kSlots) & 1, abort_flag, a.status, a.limit_ns);
-        const float l = reinterpret_cast<const float*>(smem + kOffStats)[h];
-        inv_l = (ok && l > 0.f) ? 1.f / l : 0.f;
-      }
-      ptx::tc_fence_after();
-      const bool has_rows = ok && n_tiles > 0;
-      const bool split = a.n_split > 1;
-      const int out_row0 = split ? (t * a.n_split + sp) * a.H : t * a.H;
-      uint8_t* stage_row = smem + kOffV + h * 128;
-#pragma unroll 1
-      for (int round = 0; round < (split ? 2 : 1); ++round) {
-#pragma unroll 1
-        for (int cc = 0; cc < (split ? 8 : 16); ++cc) {
-          const int c = round * 8 + cc;  // 32-column block of O
-          uint32_t o[32];
-          ptx::tmem_ld32(tmem + lane_base + c * 32, o);
-          ptx::tmem_wait_ld();
-          if (h < a.H) {
-            if (split) {
-              uint8_t* box = stage_row + cc * kQBoxBytes;
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<float4*>(box + ((e ^ (h & 7)) << 4)) =
-                    has_rows ? make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
-                                           __uint_as_float(o[4 * e + 2]) * inv_l,
-                                           __uint_as_float(o[4 * e + 3]) * inv_l)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-            } else {
-              uint8_t* box = stage_row + (c >> 1) * kQBoxBytes;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int chunk = (c & 1) * 4 + e;
-                uint4 pk = make_uint4(0, 0, 0, 0);
-                if (has_rows) {
-                  pk.x = pack_bf16(__uint_as_float(o[8 * e]) * inv_l, __uint_as_float(o[8 * e + 1]) * inv_l);
-                  pk.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv_l, __uint_as_float(o[8 * e + 3]) * inv_l);
-                  pk.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv_l, __uint_as_float(o[8 * e + 5]) * inv_l);
-                  pk.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv_l, __uint_as_float(o[8 * e + 7]) * inv_l);
-                }
-                *reinterpret_cast<uint4*>(box + ((chunk ^ (h & 7)) << 4)) = pk;
-              }
-            }
-          }
-        }
-        ptx::fence_proxy_async_smem();  // staged boxes (generic-proxy writes) -> TMA reads
-        ptx::named_sync(1, 128);
-        if (h == 0) {
-#pragma unroll 1
-          for (int b = 0; b < 8; ++b)
-            ptx::tma_store_2d_hint(&omap, ptx::smem_addr(smem + kOffV + b * kQBoxBytes),
-                                   split ? (round * 8 + b) * 32 : b * 64, out_row0, ptx::l2_evict_first_policy());
-          ptx::bulk_commit();
-          ptx::bulk_wait_read<0>();  // the staging boxes are free again (and before the CTA exits)
-        }
-        ptx::named_sync(1, 128);
-      }
+      rescale_ok = ok;
     } else if (lane == 0) {
       // ------------------------------------------------------------ slot credits back to rank 0
       for (int i = 0; i < n_tiles; ++i) {
@@ -569,6 +507,79 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_expect_tx(baddr(bars.p_full[ps]), kSlotBytes);
           ptx::mbar_arrive_cluster(ptx::map_to_rank(baddr(bars.p_empty[ps]), 0));
         }
+      }
+    }
+    if (warp >= 1 && warp < kCreditWarp) {
+      // ---- epilogue, by warps 1..16 (four per TMEM lane quarter, each with a quarter of the
+      // columns): O / l is staged as 128B-swizzled [128 x 128 B] boxes in the drained V ring (a
+      // thread writes its own row, conflict-free), then copied out row-contiguously with 16-byte
+      // stores: bf16 out (8 boxes of 64 columns) or, with a key split, the fp32 partial (16 boxes
+      // of 32 columns, in two rounds of 8).  The rescale warps first wait for the last PV product
+      // and the final statistics; a failure anywhere is voted on at the barrier.
+      const int quarter = warp & 3, grp = (warp - 1) >> 2;
+      const int h = quarter * 32 + lane;
+      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+      bool bad = false;
+      if (warp >= kRowWarp0 && n_tiles > 0) {
+        const int j = n_tiles - 1;
+        bad = !rescale_ok || !ptx::mbar_wait(baddr(bars.stats_full), 0, abort_flag, a.status, a.limit_ns) ||
+              !ptx::mbar_wait(baddr(bars.slot_free[j % kSlots]), (j / kSlots) & 1, abort_flag, a.status, a.limit_ns);
+      }
+      bad = ptx::named_sync_or(1, 512, bad);
+      const bool has_rows = !bad && n_tiles > 0;
+      const float l = has_rows ? reinterpret_cast<const float*>(smem + kOffStats)[h] : 0.f;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      ptx::tc_fence_after();
+      const bool split = a.n_split > 1;
+      const int64_t out_row0 = split ? (static_cast<int64_t>(t) * a.n_split + sp) * a.H : static_cast<int64_t>(t) * a.H;
+      const int row_bytes = split ? kDV * 4 : kDV * 2;
+      uint8_t* gout = split ? reinterpret_cast<uint8_t*>(a.part_o) : reinterpret_cast<uint8_t*>(a.out);
+      gout += out_row0 * row_bytes;
+      const uint64_t policy = ptx::l2_evict_first_policy();  // written once, read by the next stage
+      uint8_t* stage_row = smem + kOffV + h * 128;
+      const int per = split ? 2 : 4;  // 32-column blocks per warp and round
+#pragma unroll 1
+      for (int round = 0; round < (split ? 2 : 1); ++round) {
+#pragma unroll 1
+        for (int k = 0; k < per; ++k) {
+          const int cr = grp * per + k;  // block within the round
+          const int c = round * 8 + cr;  // 32-column block of O
+          uint32_t o[32];
+          ptx::tmem_ld32(tmem + lane_base + c * 32, o);
+          ptx::tmem_wait_ld();
+          if (h < a.H) {
+            if (split) {
+              uint8_t* box = stage_row + cr * kQBoxBytes;
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                *reinterpret_cast<float4*>(box + ((e ^ (h & 7)) << 4)) =
+                    make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
+                                __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l);
+            } else {
+              uint8_t* box = stage_row + (c >> 1) * kQBoxBytes;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int chunk = (c & 1) * 4 + e;
+                uint4 pk;
+                pk.x = pack_bf16(__uint_as_float(o[8 * e]) * inv_l, __uint_as_float(o[8 * e + 1]) * inv_l);
+                pk.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv_l, __uint_as_float(o[8 * e + 3]) * inv_l);
+                pk.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv_l, __uint_as_float(o[8 * e + 5]) * inv_l);
+                pk.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv_l, __uint_as_float(o[8 * e + 7]) * inv_l);
+                *reinterpret_cast<uint4*>(box + ((chunk ^ (h & 7)) << 4)) = pk;
+              }
+            }
+          }
+        }
+        ptx::named_sync(1, 512);
+        // this round's 1024 bytes of each row: chunk q = (row q / 64, 16-byte chunk q % 64)
+#pragma unroll 4
+        for (int q = (warp - 1) * 32 + lane; q < a.H * 64; q += 512) {
+          const int row = q >> 6, cc = q & 63, cb = cc & 7;
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + kOffV + (cc >> 3) * kQBoxBytes + row * 128 +
+                                                          ((cb ^ (row & 7)) << 4));
+          ptx::st_global_v4_hint(gout + static_cast<int64_t>(row) * row_bytes + round * 1024 + cc * 16, v, policy);
+        }
+        ptx::named_sync(1, 512);  // the staging boxes are free again
       }
     }
   }
@@ -615,20 +626,14 @@ cudaError_t launch_sparse_attn(const AttnArgs& a0, cudaStream_t stream) {
   if (a0.T <= 0) return cudaSuccess;
   AttnArgs a = a0;
   if (a.n_split < 1 || a.part_o == nullptr || a.part_ml == nullptr) a.n_split = 1;
-  // Q viewed as [T*H, 576] bf16 (box 64 x 128); out as [T*H, 512] bf16 (box 64 x H) or the fp32
-  // partials as [T*n_split*H, 512] (box 32 x H): a box never covers another token's rows
-  CUtensorMap qmap, omap;
+  // Q viewed as [T*H, 576] bf16, box 64 x 128 (rows past the tensor read as zero)
+  CUtensorMap qmap;
   const uint64_t rows = static_cast<uint64_t>(a.T) * a.H;
   if (!encode_tmap_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kDL, rows, kDL * 2, 64, 128))
     return cudaErrorInvalidValue;
-  const bool ok = a.n_split > 1
-                      ? encode_tmap_2d(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.part_o, kDV, rows * a.n_split, kDV * 4,
-                                       32, a.H)
-                      : encode_tmap_2d(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out, kDV, rows, kDV * 2, 64, a.H);
-  if (!ok) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<dim3(2 * a.T * a.n_split), kThreads, kSmem, stream>>>(a, qmap, omap);
+  sparse_attn_kernel<<<dim3(2 * a.T * a.n_split), kThreads, kSmem, stream>>>(a, qmap);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_split == 1) return e;
   return launch_attn_combine(a, stream);
