@@ -312,7 +312,11 @@ cudaError_t launch_t(const CUtensorMap& qm, const CUtensorMap& km, int max_keys,
     int64_t tpc = (static_cast<int64_t>(gx) * n_key_tiles + want - 1) / want;
     a.tiles_per_cta = static_cast<int>(tpc < 1 ? 1 : tpc);
   } else {
-    a.tiles_per_cta = 32;
+    // long key ranges per CTA amortise its prologue (TMEM allocation, weights, the query tile and
+    // the pipeline fill: one CTA per SM); keep at least about four CTAs per SM for balance
+    const int64_t total = static_cast<int64_t>(gx) * n_key_tiles;
+    const int64_t tpc = total / (4 * 148);
+    a.tiles_per_cta = static_cast<int>(tpc < 32 ? 32 : (tpc > 256 ? 256 : tpc));
   }
   const int gy = (n_key_tiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
   if (gx == 0 || gy == 0) return cudaSuccess;

@@ -101,6 +101,22 @@ def test_indexer_matches_oracle(dsa, cid, rows, q_pos0):
         _check_scores(sc[i, :n], ref, mass, f"cfg{cid} row {t}")
 
 
+@pytest.mark.parametrize("H_I", [8, 16, 32, 128])
+def test_indexer_head_counts(dsa, H_I):
+    # every supported prefill head count, ragged query rows (701 is not a multiple of 256 / H_I)
+    cfg = synth.config(2, H_I=H_I, L=701)
+    hinp = synth.prefill_inputs(cfg)
+    d = _cuda(hinp)
+    sc = dsa.index(d["q8"], d["q_scale"], d["w"], d["k8"], d["k_scale"])
+    assert dsa.device_status() == 0
+    sc = sc.cpu().numpy()
+    for t in [0, 1, 2, 3, 127, 128, 255, 256, 400, 699, 700]:
+        n = t + 1
+        ref = oracle.indexer_row(hinp["q8"][t], hinp["q_scale"][t], hinp["w"][t], hinp["k8"], hinp["k_scale"], n)
+        mass = _score_mass(hinp["q8"][t], hinp["q_scale"][t], hinp["w"][t], hinp["k8"], hinp["k_scale"], n)
+        _check_scores(sc[t, :n], ref, mass, f"H_I={H_I} row {t}")
+
+
 def test_indexer_paged_matches_oracle(dsa):
     cfg = synth.config(3, B=6, ctx=5000)
     hinp = synth.decode_inputs(cfg)
