@@ -219,6 +219,8 @@ def run_ours(args, dist, rank, ws):
                 "steps": max(10, args.steps), "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 / bf16",
                 "data": "synthetic", "config": {"workload": res["workload"]}, "decode": res}
+    if args.workload == "prefill128k_tail":
+        return bench_prefill_tail(dsa, synth, args, peaks)
     cid = {"prefill128k": 4, "prefill4k": 2}[args.workload]
     cfg = synth.config(cid)
     if rank:
@@ -296,6 +298,48 @@ def run_ours(args, dist, rank, ws):
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_seconds)
     return line
+
+
+def bench_prefill_tail(dsa, synth, args, peaks, n_rows=1024):
+    """The last 1024 query rows of the 128K prefill (each against ~131K keys): the steady state of
+    the 128K step at a size small enough for full profiler captures (under 1 GB on the device)."""
+    cfg = synth.config(4)
+    d = synth.prefill_tail_inputs(cfg, n_rows, device="cuda")
+    r0 = d["row0"]
+    ld = (cfg.L + 3) // 4 * 4
+    scores = torch.empty((n_rows, ld), dtype=torch.float32, device="cuda")
+    idx = torch.empty((n_rows, cfg.k), dtype=torch.int32, device="cuda")
+    out = torch.empty((n_rows, cfg.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((n_rows, cfg.H), dtype=torch.float32, device="cuda")
+    torch.cuda.empty_cache()
+    ev = {"index": [], "topk": [], "attn": []}
+
+    def step(ev=None):
+        for name, fn in (("index", lambda: dsa.index(d["q8"], d["q_scale"], d["w"], d["k8"], d["k_scale"], q_pos0=r0,
+                                                      scores=scores)),
+                         ("topk", lambda: dsa.topk(scores, cfg.k, q_pos0=r0, n_cols=cfg.L, idx=idx)),
+                         ("attn", lambda: dsa.sparse_attn(d["q"], d["kv"], idx, cfg.scale, out=out, lse=lse))):
+            if ev is not None:
+                ev[name].append(_rec())
+            fn()
+            if ev is not None:
+                ev[name].append(_rec())
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    for _ in range(args.steps):
+        step(ev)
+    torch.cuda.synchronize()
+    st = dsa.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+    kms = {k: round(_pairs_ms(v) / args.steps, 4) for k, v in ev.items()}
+    ms = sum(kms.values())
+    return {"metric": "prefill tail tokens/s", "value": round(n_rows / (ms * 1e-3), 1), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "dtype": "fp8-e4m3 / bf16", "data": "synthetic",
+            "config": {"workload": f"prefill L={cfg.L}: query rows {r0}..{cfg.L - 1}, k=2048, H=128, H_I=64"},
+            "kernels_ms": kms}
 
 
 def bench_decode(dsa, synth, args, peaks, cid=5):
@@ -494,8 +538,8 @@ def main():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--chunk", type=int, default=8192)
-    p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k", "decode", "decode32k"],
-                   help="prefill4k / decode / decode32k run single pieces (used for profiler captures)")
+    p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k", "prefill128k_tail", "decode", "decode32k"],
+                   help="the others run single pieces (used for profiler captures)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")

@@ -173,6 +173,46 @@ def prefill_inputs(cfg: Config, device="cpu") -> dict:
     return {n: t.to(device).contiguous() for n, t in out.items()}
 
 
+def _randn_rows(cfg, tid, shape, r0, r1, device, rows_per_chunk, dtype=torch.float32):
+    """Rows [r0, r1) of _randn(cfg, tid, shape, device, rows_per_chunk, dtype), drawing only the
+    chunks that cover them (bit-identical to the same rows of the full draw)."""
+    out = []
+    for c in range(r0 // rows_per_chunk, (r1 - 1) // rows_per_chunk + 1):
+        c0 = c * rows_per_chunk
+        c1 = min(shape[0], c0 + rows_per_chunk)
+        x = torch.randn((c1 - c0,) + tuple(shape[1:]), generator=_gen(cfg, tid, device, c), device=device).to(dtype)
+        out.append(x[max(r0, c0) - c0:min(r1, c1) - c0])
+    return torch.cat(out)
+
+
+def prefill_tail_inputs(cfg: Config, n_rows: int, device="cuda") -> dict:
+    """The last n_rows query rows of a large prefill workload (L > 8192) with its full key side.
+
+    Keys (k8, k_scale, kv) are those of prefill_inputs; the query-side tensors (q8, q_scale, w,
+    q) are the rows [L - n_rows, L) of prefill_inputs, drawn without the rest.  For workloads
+    without planted keys only (planting couples keys to every query).  Adds row0 = L - n_rows.
+    """
+    assert cfg.mode == "prefill" and cfg.L > 8192 and cfg.planted == 0
+    L, H_I, H = cfg.L, cfg.H_I, cfg.H
+    r0 = L - n_rows
+    qI = _randn_rows(cfg, 1, (L, H_I, D_INDEX), r0, L, device, 4096)
+    kI = _randn(cfg, 2, (L, D_INDEX), device, 4096)
+    if cfg.lognormal_keys:
+        g = torch.exp(0.5 * _randn(cfg, 3, (L,), device))
+        kI *= g[:, None]
+    w = (_randn(cfg, 5, (L, H_I), device) / math.sqrt(H_I))[r0:]
+    q8, sq = encode_e4m3_per_token(qI)
+    k8, sk = encode_e4m3_per_token(kI)
+    del qI, kI
+    q = _randn_rows(cfg, 6, (L, H, D_LATENT), r0, L, device, 2048, torch.bfloat16)
+    kv = _randn(cfg, 7, (L, D_LATENT), device, 4096, torch.bfloat16)
+    out = dict(q8=q8, q_scale=sq[:, None].expand(n_rows, H_I).contiguous(), w=w.float(), k8=k8, k_scale=sk, q=q,
+               kv=kv)
+    out = {n: t.to(device).contiguous() for n, t in out.items()}
+    out["row0"] = r0
+    return out
+
+
 def decode_inputs(cfg: Config, device="cpu") -> dict:
     """All inputs of one decode step over a paged cache, on `device`.
 
