@@ -269,8 +269,17 @@ def run_ours(args, dist, rank, ws):
         v["frac"] = v["achieved"] / v["peak"]
     dom_name = max(kern, key=lambda n: kern[n]["ms"])
     dom = kern[dom_name]
+    # DRAM bytes (read + write) per query row from the ncu capture of the 1024-row 128K tail
+    # (profiles/prefill128k_tail_full.md), scaled to the launch's rows; the capture starts from a
+    # flushed L2, so it overstates the steady state a little.  None where no capture matches.
+    traffic_per_row = {"sparse_attn": (0.422053e9 + 0.1166912e9) / 1024, "indexer": (0.063149e9 + 0.475974e9) / 1024,
+                       "topk": (1.053748e9 + 0.007288e9) / 1024}
+    traffic = traffic_per_row.get(dom_name)
+    if traffic is not None:
+        traffic = round(traffic * cfg.L / kern[dom_name]["launches"])
     roofline = {"kernel": dom_name, "bound": dom["bound"], "achieved": round(dom["achieved"], 2),
-                "peak": dom["peak"], "unit": dom["unit"], "frac": round(dom["frac"], 4), "traffic": None,
+                "peak": dom["peak"], "unit": dom["unit"], "frac": round(dom["frac"], 4), "traffic": traffic,
+                "traffic_unit": "bytes per launch (ncu dram read + write, scaled from the 128K tail capture)",
                 "peak_source": f"{peaks['src']} (sustained; FP8 = 2 x bf16)" if dom["unit"] == "TFLOP/s"
                 else f"{peaks['src']} copy bandwidth"}
 
