@@ -42,6 +42,10 @@ struct IndexerArgs {
 cudaError_t launch_indexer(const uint8_t* q8, const uint8_t* k8, int64_t n_key_rows, int H_I, bool paged,
                            int max_keys, const IndexerArgs& a, cudaStream_t stream);
 int indexer_supported_heads(int H_I, bool paged);
+// The decode (paged) kernel: q8 as [rows * H_I, 128] (box H_I rows), the key cache as
+// [n_pages * page_size, 128] (box page_size rows).
+cudaError_t launch_indexer_paged(const CUtensorMap& qm, const CUtensorMap& km, int H_I, int max_keys,
+                                 const IndexerArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- top-k
 

@@ -2,10 +2,10 @@
 //     I[t,s] = sum_j w[t,j] * ReLU(q^I[t,j] . k^I[s])
 // on FP8 e4m3 inputs with per-token scales, over the preceding keys s <= t.
 //
-// One tensor-core tile is D[128 keys x N] = K8[128 x 128] * Q8[N x 128]^T, where the N
-// columns are (token, head) pairs: 256 / H_I tokens x H_I heads in prefill, one token x
-// H_I heads in decode.  Keys sit on the TMEM lanes, so the head-weighted ReLU sum for a
-// (token, key) pair runs down one thread's registers with no cross-thread reduction.
+// One tensor-core tile is D[128 keys x 256] = K8[128 x 128] * Q8[256 x 128]^T, where the 256
+// columns are (token, head) pairs: 256 / H_I tokens x H_I heads.  Keys sit on the TMEM lanes,
+// so the head-weighted ReLU sum for a (token, key) pair runs down one thread's registers with no
+// cross-thread reduction.  (The decode indexer over a paged cache is in indexer_paged.cu.)
 //
 // Warp roles (320 threads):
 //   warp 0      TMA producer: the query tile once, then key tiles through a ring of stages
@@ -26,12 +26,12 @@ constexpr int kThreads = 320;
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 __host__ __device__ constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
-template <int HI, bool PAGED>
+template <int HI>
 struct IdxCfg {
-  static constexpr int NCOL = PAGED ? HI : 256;
+  static constexpr int NCOL = 256;
   static constexpr int TT = NCOL / HI;
   static constexpr int NACC = (TT >= 32) ? 1 : ((32 / TT) < 4 ? (32 / TT) : 4);
-  static constexpr int STAGES = 6;  // decode: small enough for two CTAs per SM
+  static constexpr int STAGES = 6;
   static constexpr int Q_BYTES = NCOL * kRowBytes;
   static constexpr int TMEM_COLS = pow2_cols(2 * NCOL);
   static constexpr int OFF_Q = 0;
@@ -52,32 +52,22 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int HI, bool PAGED>
-__global__ void __launch_bounds__(kThreads, PAGED ? 2 : 1)
+template <int HI>
+__global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const IndexerArgs a) {
-  using C = IdxCfg<HI, PAGED>;
+  using C = IdxCfg<HI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- this CTA's work: query rows [row0, row0 + TT) (or sequence b) x key tiles [tb, te)
-  int row0, key_end;
-  if (PAGED) {
-    row0 = blockIdx.x;
-    key_end = a.seq_lens[row0];
-    if (key_end < 0 || key_end > a.S) {  // a.S = max_seq_len: the score row and block-table row bound
-      if (threadIdx.x == 0 && blockIdx.y == 0) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
-      key_end = key_end < 0 ? 0 : a.S;
-    }
-  } else {
-    row0 = blockIdx.x * C::TT;
-    const int rlast = min(a.rows, row0 + C::TT) - 1;
-    const int64_t e = a.q_pos0 + rlast + 1;
-    key_end = static_cast<int>(e < a.S ? e : a.S);
-  }
+  // ---- this CTA's work: query rows [row0, row0 + TT) x key tiles [tb, te)
+  const int row0 = blockIdx.x * C::TT;
+  const int rlast = min(a.rows, row0 + C::TT) - 1;
+  const int64_t e = a.q_pos0 + rlast + 1;
+  const int key_end = static_cast<int>(e < a.S ? e : a.S);
   const int n_tiles_all = (key_end + kTileKeys - 1) / kTileKeys;
   const int tb = blockIdx.y * a.tiles_per_cta;
   const int te = min(n_tiles_all, tb + a.tiles_per_cta);
@@ -124,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, PAGED ? 2 : 1)
       const int tt = i / HI, j = i % HI;
       const int r = row0 + tt;
       float v = 0.f;
-      if (PAGED || r < a.rows) {
+      if (r < a.rows) {
         const int64_t o = static_cast<int64_t>(r) * HI + j;
         v = a.w[o] * a.q_scale[o];
       }
@@ -148,31 +138,8 @@ __global__ void __launch_bounds__(kThreads, PAGED ? 2 : 1)
         if (!ptx::mbar_wait(k_empty(st), ph ^ 1, abort_flag, a.status, a.limit_ns)) break;
         const int s0 = (tb + i) * kTileKeys;
         const uint32_t dst = sK + st * kKeyTileBytes;
-        if (!PAGED) {
-          ptx::mbar_arrive_expect_tx(k_full(st), kKeyTileBytes);
-          ptx::tma_load_2d(dst, &kmap, k_full(st), 0, s0);
-        } else {
-          const int pg = a.page_size, per = kTileKeys / pg;
-          const int32_t* bt = a.block_table + static_cast<int64_t>(row0) * a.bt_stride;
-          uint32_t nbytes = 0;
-          for (int u = 0; u < per; ++u) {
-            const int p = s0 / pg + u;
-            if (p * pg < key_end) {
-              const int32_t phys = bt[p];
-              if (phys >= 0 && phys < a.n_pages) nbytes += pg * kRowBytes;
-              else atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
-            }
-          }
-          ptx::mbar_arrive_expect_tx(k_full(st), nbytes);
-          for (int u = 0; u < per; ++u) {
-            const int p = s0 / pg + u;
-            if (p * pg < key_end) {
-              const int32_t phys = bt[p];
-              if (phys >= 0 && phys < a.n_pages)
-                ptx::tma_load_2d(dst + u * pg * kRowBytes, &kmap, k_full(st), 0, phys * pg);
-            }
-          }
-        }
+        ptx::mbar_arrive_expect_tx(k_full(st), kKeyTileBytes);
+        ptx::tma_load_2d(dst, &kmap, k_full(st), 0, s0);
         ++issued;
       }
       if (*abort_flag) {
@@ -214,33 +181,18 @@ __global__ void __launch_bounds__(kThreads, PAGED ? 2 : 1)
     const int g = (warp - 2) >> 2;  // tiles i = g mod 2 use TMEM buffer g
     const int sub = warp & 3;       // this warp may touch TMEM lanes [32*sub, 32*sub + 32)
     const int row = sub * 32 + lane;
-    // This group handles tiles g, g+2, g+4, ...  The key's page entry (decode) is fetched four tiles
-    // ahead and its scale two tiles ahead, so neither dependent load stalls the tile being finished.
+    // This group handles tiles g, g+2, g+4, ...; the key scale of a tile is loaded one tile (of the
+    // group) ahead so its latency does not land on the tile being finished.
     auto key_of = [&](int i) { return (tb + i) * kTileKeys + row; };
-    auto page_of = [&](int i) -> int32_t {  // physical page of this thread's key in tile i, or -1
+    auto scale_of = [&](int i) -> float {  // 0 for a key past the range
       const int s = key_of(i);
-      if (i >= n_tiles || s >= key_end) return -1;
-      const int32_t phys = a.block_table[static_cast<int64_t>(row0) * a.bt_stride + s / a.page_size];
-      return (phys >= 0 && phys < a.n_pages) ? phys : -1;
+      return (i < n_tiles && s < key_end) ? a.k_scale[s] : 0.f;
     };
-    auto scale_of = [&](int i, int32_t phys) -> float {  // 0 marks an invalid key
-      const int s = key_of(i);
-      if (i >= n_tiles || s >= key_end) return 0.f;
-      if (PAGED) return phys < 0 ? 0.f : a.k_scale[static_cast<int64_t>(phys) * a.page_size + s % a.page_size];
-      return a.k_scale[s];
-    };
-    int32_t page_a = PAGED ? page_of(g) : 0, page_b = PAGED ? page_of(g + 2) : 0;
-    float sk_next = PAGED ? scale_of(g, page_a) : 0.f;
+    float sk_next = scale_of(g);
     for (int i = g; i < n_tiles; i += 2) {
-      // prefill: one contiguous scale load per key (cheap, issued here); decode: pipelined lookups
-      const float sk = PAGED ? sk_next : scale_of(i, 0);
-      const bool kvalid = key_of(i) < key_end && (!PAGED || page_a >= 0);
-      if (PAGED) {
-        const int32_t page_c = page_of(i + 4);
-        sk_next = scale_of(i + 2, page_b);
-        page_a = page_b;
-        page_b = page_c;
-      }
+      const float sk = sk_next;
+      sk_next = scale_of(i + 2);
+      const bool kvalid = key_of(i) < key_end;
       const int s = key_of(i);
       const uint32_t bph = (i >> 1) & 1;
       if (!ptx::mbar_wait(t_full(g), bph, abort_flag, a.status, a.limit_ns)) break;
@@ -282,9 +234,7 @@ __global__ void __launch_bounds__(kThreads, PAGED ? 2 : 1)
 #pragma unroll
         for (int e = 1; e < C::NACC; ++e) sum += acc[tt][e];
         const int r = row0 + tt;
-        if (PAGED) {
-          if (s < key_end) a.scores[static_cast<int64_t>(r) * a.ld + s] = kvalid ? sum * sk : -INFINITY;
-        } else if (kvalid && r < a.rows && s <= a.q_pos0 + r) {
+        if (kvalid && r < a.rows && s <= a.q_pos0 + r) {
           a.scores[static_cast<int64_t>(r) * a.ld + s] = sum * sk;
         }
       }
@@ -299,28 +249,21 @@ __global__ void __launch_bounds__(kThreads, PAGED ? 2 : 1)
   }
 }
 
-template <int HI, bool PAGED>
+template <int HI>
 cudaError_t launch_t(const CUtensorMap& qm, const CUtensorMap& km, int max_keys, const IndexerArgs& a0,
                      cudaStream_t stream) {
-  using C = IdxCfg<HI, PAGED>;
+  using C = IdxCfg<HI>;
   IndexerArgs a = a0;
   const int n_key_tiles = (max_keys + kTileKeys - 1) / kTileKeys;
-  const int gx = PAGED ? a.rows : (a.rows + C::TT - 1) / C::TT;
-  if (PAGED) {
-    // spread a batch's keys over about eight CTAs per SM (two resident at a time)
-    const int64_t want = 8 * 148;
-    int64_t tpc = (static_cast<int64_t>(gx) * n_key_tiles + want - 1) / want;
-    a.tiles_per_cta = static_cast<int>(tpc < 1 ? 1 : tpc);
-  } else {
-    // long key ranges per CTA amortise its prologue (TMEM allocation, weights, the query tile and
-    // the pipeline fill: one CTA per SM); keep at least about four CTAs per SM for balance
-    const int64_t total = static_cast<int64_t>(gx) * n_key_tiles;
-    const int64_t tpc = total / (4 * 148);
-    a.tiles_per_cta = static_cast<int>(tpc < 32 ? 32 : (tpc > 256 ? 256 : tpc));
-  }
+  const int gx = (a.rows + C::TT - 1) / C::TT;
+  // long key ranges per CTA amortise its prologue (TMEM allocation, weights, the query tile and
+  // the pipeline fill: one CTA per SM); keep at least about four CTAs per SM for balance
+  const int64_t total = static_cast<int64_t>(gx) * n_key_tiles;
+  const int64_t tpc = total / (4 * 148);
+  a.tiles_per_cta = static_cast<int>(tpc < 32 ? 32 : (tpc > 256 ? 256 : tpc));
   const int gy = (n_key_tiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
   if (gx == 0 || gy == 0) return cudaSuccess;
-  auto kern = indexer_kernel<HI, PAGED>;
+  auto kern = indexer_kernel<HI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<dim3(gx, gy), kThreads, C::SMEM, stream>>>(qm, km, a);
@@ -350,21 +293,17 @@ cudaError_t launch_indexer(const uint8_t* q8, const uint8_t* k8, int64_t n_key_r
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d_u8(&km, k8, kRowBytes, n_key_rows, kRowBytes, paged ? a.page_size : kTileKeys))
     return cudaErrorInvalidValue;
-#define DSA_IDX_CASE(HV)                                                       \
-  case HV:                                                                     \
-    return paged ? launch_t<HV, true>(qm, km, max_keys, a, stream)             \
-                 : launch_t<HV, false>(qm, km, max_keys, a, stream);
   if (!indexer_supported_heads(H_I, paged)) return cudaErrorInvalidValue;
+  if (paged) return launch_indexer_paged(qm, km, H_I, max_keys, a, stream);
   switch (H_I) {
-    DSA_IDX_CASE(64)
-    DSA_IDX_CASE(128)
-    case 4: return launch_t<4, false>(qm, km, max_keys, a, stream);
-    case 8: return launch_t<8, false>(qm, km, max_keys, a, stream);
-    case 16: return launch_t<16, false>(qm, km, max_keys, a, stream);
-    case 32: return launch_t<32, false>(qm, km, max_keys, a, stream);
+    case 64: return launch_t<64>(qm, km, max_keys, a, stream);
+    case 128: return launch_t<128>(qm, km, max_keys, a, stream);
+    case 4: return launch_t<4>(qm, km, max_keys, a, stream);
+    case 8: return launch_t<8>(qm, km, max_keys, a, stream);
+    case 16: return launch_t<16>(qm, km, max_keys, a, stream);
+    case 32: return launch_t<32>(qm, km, max_keys, a, stream);
     default: return cudaErrorInvalidValue;
   }
-#undef DSA_IDX_CASE
 }
 
 }  // namespace dsa

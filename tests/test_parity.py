@@ -117,6 +117,28 @@ def test_indexer_head_counts(dsa, H_I):
         _check_scores(sc[t, :n], ref, mass, f"H_I={H_I} row {t}")
 
 
+@pytest.mark.parametrize("B,lo,hi,H_I", [(40, 1, 3000, 64), (9, 100, 20000, 128), (300, 1, 700, 64)])
+def test_indexer_paged_mixed_lengths(dsa, B, lo, hi, H_I):
+    # many sequences per CTA share (segments), sequences shorter than one 128-key tile, both head counts
+    cfg = synth.config(5, B=B, ctx_lo=lo, ctx_hi=hi, H_I=H_I, planted=2)
+    hinp = synth.decode_inputs(cfg)
+    d = _cuda(hinp)
+    max_len = int(hinp["seq_lens"].max())
+    sc = dsa.index_paged(d["q8"], d["q_scale"], d["w"], d["k8_cache"], d["k_scale_cache"], d["block_table"],
+                         d["seq_lens"], max_len)
+    assert dsa.device_status() == 0
+    sc = sc.cpu().numpy()
+    page = cfg.page
+    for b in sorted(set([0, 1, B // 2, B - 2, B - 1])):
+        n = int(hinp["seq_lens"][b])
+        k8 = oracle.decode_gather(hinp["k8_cache"], hinp["block_table"][b], n, page)
+        ks = oracle.decode_gather(hinp["k_scale_cache"], hinp["block_table"][b], n, page)
+        ref = oracle.indexer_row(hinp["q8"][b], hinp["q_scale"][b], hinp["w"][b], k8, ks, n)
+        mass = _score_mass(hinp["q8"][b], hinp["q_scale"][b], hinp["w"][b], torch.as_tensor(k8),
+                           torch.as_tensor(ks), n)
+        _check_scores(sc[b, :n], ref, mass, f"paged B={B} seq {b}")
+
+
 def test_indexer_paged_matches_oracle(dsa):
     cfg = synth.config(3, B=6, ctx=5000)
     hinp = synth.decode_inputs(cfg)
