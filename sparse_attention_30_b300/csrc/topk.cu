@@ -17,6 +17,7 @@
 #include <math.h>
 
 #include "dsa_internal.h"
+#include "dsa_ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -28,6 +29,12 @@ constexpr int kCandCap = 6144;
 constexpr int kSample = 4096;  // held in cand_key until the filter pass starts
 constexpr int kUnroll = 8;     // float4 loads in flight per thread in the filter pass
 static_assert(kSample <= kCandCap, "the sample is staged in the candidate buffer");
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x);
@@ -156,38 +163,37 @@ __device__ void select_from_candidates(TopkSmem& s, uint32_t count, uint32_t k, 
   }
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  TopkSmem& s = *reinterpret_cast<TopkSmem*>(smem_raw);
-  const int t = blockIdx.x;
-  const int tid = threadIdx.x;
+// Row t's length (columns that take part in the selection).
+__device__ __forceinline__ int row_length(const TopkArgs& a, int t) {
   int64_t n64 = a.row_lens ? static_cast<int64_t>(a.row_lens[t]) : a.q_pos0 + t + 1;
   if (!a.row_lens && n64 > a.n_cols) n64 = a.n_cols;
   if (n64 > a.ld) n64 = a.ld;
   if (n64 < 0) n64 = 0;
-  const int n = static_cast<int>(n64);
-  const uint32_t k = static_cast<uint32_t>(a.k);
-  int32_t* out = a.idx + static_cast<int64_t>(t) * a.k;
-  const float* row = a.scores + static_cast<int64_t>(t) * a.ld;  // 16-byte aligned rows
+  return static_cast<int>(n64);
+}
 
+// Rows with n <= kCandCap: every position (n <= k), or one read into shared memory and the exact
+// selection there.
+__device__ void short_row(TopkSmem& s, const float* row, int n, uint32_t k, int32_t* out, int k_slots) {
+  const int tid = threadIdx.x;
   if (static_cast<uint32_t>(n) <= k) {
-    for (int i = tid; i < a.k; i += kThreads) out[i] = i < n ? i : -1;
+    for (int i = tid; i < k_slots; i += kThreads) out[i] = i < n ? i : -1;
     return;
   }
   if (tid == 0) { s.n_out = 0; s.n_cand = 0; s.n_eq = 0; }
-
-  if (n <= kCandCap) {
-    // the whole row fits: one read, exact selection in shared memory
-    for (int i = tid; i < n; i += kThreads) {
-      s.cand_key[i] = order_key(row[i]);
-      s.cand_pos[i] = i;
-    }
-    __syncthreads();
-    select_from_candidates(s, n, k, out);
-    return;
+  for (int i = tid; i < n; i += kThreads) {
+    s.cand_key[i] = order_key(row[i]);
+    s.cand_pos[i] = i;
   }
+  __syncthreads();
+  select_from_candidates(s, n, k, out);
+}
 
-  // ---- sample: kSample keys at evenly spread positions; tau = the sample's rank-r key
+// The sample's lower bound: kSample keys at evenly spread positions, tau = the sample's rank-r
+// key, returned as a float bound.  {x >= tau_f} is a prefix of the key order for non-NaN x (it
+// takes both zeros or neither), so it holds the row's top k whenever it has k members.
+__device__ float sample_bound(TopkSmem& s, const float* row, int n, uint32_t k) {
+  const int tid = threadIdx.x;
   {
     constexpr int kPer = kSample / kThreads;
     float v[kPer];
@@ -207,21 +213,22 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
         for (int i = tid; i < kSample; i += kThreads) f(s.cand_key[i]);
       },
       &tau, &unused);
-  // keys >= tau as a float bound: {x >= tau_f} is a prefix of the key order for non-NaN x
-  // (it takes both zeros or neither), so it holds the row's top k whenever it has k members
-  const float tau_f = __uint_as_float((tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau);
+  return __uint_as_float((tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau);
+}
 
-  // ---- filter: compact the positions with x >= tau_f (counting those beyond capacity)
-  const int n4 = n >> 2;
+// Compacts the positions p in [p0, p1) (p0 a multiple of 4) with row[p] >= tau_f into the
+// candidate buffer; s.n_cand counts them all, including those beyond its capacity.
+__device__ void filter_range(TopkSmem& s, const float* row, int p0, int p1, float tau_f) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int q0 = p0 >> 2, q1 = p1 >> 2;
   const float4* row4 = reinterpret_cast<const float4*>(row);
-  const int lane = tid & 31;
-  for (int b = 0; b < n4; b += kThreads * kUnroll) {  // block-uniform trip count
+  for (int b = q0; b < q1; b += kThreads * kUnroll) {  // block-uniform trip count
     const int i0 = b + tid;
     float4 v[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 + u * kThreads;
-      v[u] = i < n4 ? __ldcs(row4 + i) : make_float4(NAN, NAN, NAN, NAN);  // NaN never passes
+      v[u] = i < q1 ? __ldcs(row4 + i) : make_float4(NAN, NAN, NAN, NAN);  // NaN never passes
     }
     uint32_t mask = 0;  // bit 4u + c: element c of v[u]
 #pragma unroll
@@ -253,18 +260,16 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
       ++base;
     }
   }
-  for (int i = (n4 << 2) + tid; i < n; i += kThreads) {
+  for (int i = (q1 << 2) + tid; i < p1; i += kThreads) {
     const float x = row[i];
     append(&s.n_cand, s.cand_pos, kCandCap, x >= tau_f, i, order_key(x), s.cand_key);
   }
-  __syncthreads();
-  const uint32_t found = s.n_cand;
-  if (found >= k && found <= static_cast<uint32_t>(kCandCap)) {
-    select_from_candidates(s, found, k, out);
-    return;
-  }
+}
 
-  // ---- fallback: radix select over the whole row, re-read from global memory
+// Radix select over the whole row, re-read from global memory (the general fallback).
+__device__ void full_row_select(TopkSmem& s, const float* row, int n, uint32_t k, int32_t* out) {
+  const int tid = threadIdx.x;
+  if (tid == 0) { s.n_out = 0; s.n_eq = 0; }
   uint32_t thr, n_equal;
   radix_threshold(
       s, k,
@@ -280,15 +285,118 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  TopkSmem& s = *reinterpret_cast<TopkSmem*>(smem_raw);
+  const int t = blockIdx.x;
+  const int n = row_length(a, t);
+  const uint32_t k = static_cast<uint32_t>(a.k);
+  int32_t* out = a.idx + static_cast<int64_t>(t) * a.k;
+  const float* row = a.scores + static_cast<int64_t>(t) * a.ld;  // 16-byte aligned rows
+  if (n <= kCandCap) {
+    short_row(s, row, n, k, out, a.k);
+    return;
+  }
+  if (threadIdx.x == 0) { s.n_out = 0; s.n_cand = 0; s.n_eq = 0; }
+  const float tau_f = sample_bound(s, row, n, k);
+  filter_range(s, row, 0, n, tau_f);
+  __syncthreads();
+  const uint32_t found = s.n_cand;
+  if (found >= k && found <= static_cast<uint32_t>(kCandCap)) select_from_candidates(s, found, k, out);
+  else full_row_select(s, row, n, k, out);
+}
+
+// Few long rows (decode): a cluster of `cluster` CTAs per row.  Every CTA derives the same bound
+// from the same sample and filters its 1/cluster of the row into its own candidate buffer; rank 0
+// gathers the candidates through distributed shared memory and selects.  A rank-0 fallback (the
+// whole row) covers a sample that missed or overflowing candidates.
+__global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  TopkSmem& s = *reinterpret_cast<TopkSmem*>(smem_raw);
+  const uint32_t rank = ptx::cluster_ctarank();
+  uint32_t csize;
+  asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+  const int t = blockIdx.x / csize;
+  const int n = row_length(a, t);
+  const uint32_t k = static_cast<uint32_t>(a.k);
+  int32_t* out = a.idx + static_cast<int64_t>(t) * a.k;
+  const float* row = a.scores + static_cast<int64_t>(t) * a.ld;
+  if (n <= kCandCap) {  // uniform over the cluster: rank 0 alone, no cluster barrier
+    if (rank == 0) short_row(s, row, n, k, out, a.k);
+    return;
+  }
+  if (threadIdx.x == 0) { s.n_out = 0; s.n_cand = 0; s.n_eq = 0; }
+  const float tau_f = sample_bound(s, row, n, k);
+  const int seg = ((n + 4 * static_cast<int>(csize) - 1) / (4 * static_cast<int>(csize))) * 4;
+  const int p0 = min(n, static_cast<int>(rank) * seg), p1 = min(n, p0 + seg);
+  filter_range(s, row, p0, p1, tau_f);
+  __syncthreads();
+  ptx::cluster_sync_all();  // every rank's candidates are complete and visible to the cluster
+  __shared__ uint32_t base_of[8], total_s;
+  __shared__ int overflow_s;
+  if (rank == 0 && threadIdx.x == 0) {
+    uint32_t total = 0;
+    int overflow = 0;
+    for (uint32_t r = 0; r < csize; ++r) {
+      const uint32_t c = r == 0 ? s.n_cand : ld_cluster_u32(ptx::map_to_rank(ptx::smem_addr(&s.n_cand), r));
+      if (c > static_cast<uint32_t>(kCandCap)) overflow = 1;
+      base_of[r] = total;
+      total += c;
+    }
+    total_s = total;
+    overflow_s = overflow || total > static_cast<uint32_t>(kCandCap) || total < k;
+  }
+  __syncthreads();
+  if (rank == 0 && !overflow_s) {
+    // append the other ranks' candidates after rank 0's own
+    for (uint32_t r = 1; r < csize; ++r) {
+      const uint32_t b = base_of[r], c = (r + 1 < csize ? base_of[r + 1] : total_s) - b;
+      const uint32_t kr = ptx::map_to_rank(ptx::smem_addr(s.cand_key), r);
+      const uint32_t pr = ptx::map_to_rank(ptx::smem_addr(s.cand_pos), r);
+      for (uint32_t i = threadIdx.x; i < c; i += kThreads) {
+        s.cand_key[b + i] = ld_cluster_u32(kr + 4 * i);
+        s.cand_pos[b + i] = static_cast<int32_t>(ld_cluster_u32(pr + 4 * i));
+      }
+    }
+  }
+  __syncthreads();
+  ptx::cluster_sync_all();  // the other ranks' shared memory is no longer read after this point
+  if (rank != 0) return;
+  if (!overflow_s) select_from_candidates(s, total_s, k, out);
+  else full_row_select(s, row, n, k, out);
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
   const int smem = static_cast<int>(sizeof(TopkSmem));
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // rows spread over clusters when there are too few rows to fill the GPU (decode)
+  int csize = 1;
+  while (csize < 8 && a.T * csize * 2 <= sms) csize *= 2;
+  if (csize == 1 || a.ld <= kCandCap) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<<<a.T, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  topk_kernel<<<a.T, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.T * csize);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a);
 }
 
 }  // namespace dsa

@@ -211,6 +211,29 @@ def test_topk_exact_on_fixed_scores(dsa, dist, n, k):
         assert np.all(idx[r, min(k, nr):] == -1)
 
 
+@pytest.mark.parametrize("dist", ["normal", "ties", "spikes", "const"])
+def test_topk_many_long_rows(dsa, dist):
+    # 80 rows: one CTA per row (few rows are spread over clusters instead); long rows take the
+    # sample-and-filter path, ties and spikes its fallback
+    rng = np.random.default_rng(5)
+    T, n, k = 80, 20000, 2048
+    if dist == "normal":
+        v = rng.standard_normal((T, n))
+    elif dist == "ties":
+        v = rng.integers(0, 4, (T, n)).astype(np.float64)
+    elif dist == "const":
+        v = np.full((T, n), -2.5)
+    else:
+        v = rng.random((T, n))
+        v[:, (np.arange(4096) * n) // 4096] += 100.0
+    v = v.astype(np.float32)
+    lens = torch.tensor([n - 7 * t for t in range(T)], dtype=torch.int32)
+    idx = dsa.topk(torch.from_numpy(v).cuda(), k, row_lens=lens.cuda()).cpu().numpy()
+    assert dsa.device_status() == 0
+    for t in range(0, T, 7):
+        _topk_valid(v[t, :int(lens[t])].astype(np.float64), idx[t], k)
+
+
 def test_topk_causal_prefix_rows(dsa):
     rng = np.random.default_rng(3)
     T, S, k, q_pos0 = 300, 5000, 2048, 1900
