@@ -70,6 +70,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait for waiters off the critical path: sleeps between polls so that the spinning warp
+// does not take issue slots from the warps it shares a scheduler with.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                int* status, uint64_t limit_ns, uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicCAS(status, 0, DSA_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- clusters / distributed shared memory
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

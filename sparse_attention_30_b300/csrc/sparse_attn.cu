@@ -4,24 +4,29 @@
 // Every head of token t sees the same rows c_s, so per token this is a dense
 // [H x 576] x [576 x |S_t|] product followed by [H x |S_t|] x [|S_t| x 512].
 //
-// One token runs on a cluster of two CTAs with different jobs, and data flows one way:
+// A cluster of two CTAs with different jobs works through a list of work items (a token, or with
+// a key split one share of a token's selected tiles), one after another, and data flows one way:
 //
 //   rank 0, "score" CTA: Q [128 x 576] bf16 sits in TMEM (A operand of the MMA read straight
 //     from tensor memory); S = Q K^T is computed 64 keys at a time (N = 64) into two TMEM
 //     buffers from K rows that twelve cp.async warps gather into a 2-stage ring; four warps
 //     (one head row per thread) run the online softmax.  Each 64-key tile of P (bf16) plus
 //     per-row rescale factors is pushed into rank 1's shared memory with an asynchronous bulk
-//     copy.
+//     copy, and an item's final row statistics follow its last tile.
 //   rank 1, "value" CTA: O [128 x 512] fp32 fills its whole TMEM; twelve warps gather the value
 //     part (first 512 latent dims) of the same rows into a 2-stage ring and O += P V runs as soon
 //     as a P tile lands.  When rank 0 moved a row's running max (lazily: only when it grows by
 //     more than 2^8), the factor travels with P and O is rescaled before that tile's PV.  Ring
 //     slots are handed back to rank 0 by a credit warp, off the critical path.
 //
-// Nothing is computed twice and nothing waits on a round trip between the CTAs; the MMA work is
-// 576 (S) vs 512 (PV) latent dims per key on the two SMs.  MMAs are issued warp-uniformly
-// (one elected lane), and tiles are 64 keys wide, because narrow or single-thread-issued
-// tcgen05.mma chains are issue-bound rather than tensor-bound.
+// Items follow each other without a pause in either pipeline: rank 0 loads the next item's Q
+// into its K ring as soon as the last S product of the previous item has completed (twelve
+// warps move it into TMEM), while rank 1 still finishes that item's PV products and writes its
+// output; rank 1's next PV product waits only until O has been read out.  A scheduler warp in
+// each CTA finds every item's tile count (the first empty slot of its index row) ahead of time
+// and hands items to the other warps through a small ring.  MMAs are issued warp-uniformly (one
+// elected lane), and tiles are 64 keys wide, because narrow or single-thread-issued tcgen05.mma
+// chains are issue-bound rather than tensor-bound.
 #include <cuda_bf16.h>
 
 #include "dsa_internal.h"
@@ -34,10 +39,11 @@ constexpr int kProdWarps = 12;                 // warps 1..12 gather
 constexpr int kProducers = kProdWarps * 32;
 constexpr int kRowWarp0 = 1 + kProdWarps;      // warps 13..16: one head row per thread (TMEM lane)
 constexpr int kCreditWarp = kRowWarp0 + 4;     // warp 17 (rank 1): slot credits
-constexpr int kThreads = 32 * (kCreditWarp + 1);
+constexpr int kSchedWarp = kCreditWarp + 1;    // warp 18: work items
+constexpr int kThreads = 32 * (kSchedWarp + 1);
 constexpr int kKT = 64;                        // keys per tile
 constexpr int kDL = 576, kDV = 512;
-constexpr int kKStages = 2, kVStages = 2, kSlots = 4, kSBufs = 2;
+constexpr int kKStages = 2, kVStages = 2, kSlots = 4, kSBufs = 2, kSched = 4;
 constexpr int kBlockBytes = kKT * 128;         // 64 rows x 64 bf16
 constexpr int kKStageBytes = 9 * kBlockBytes;  // 72 KB: all 576 dims
 constexpr int kVStageBytes = 8 * kBlockBytes;  // 64 KB: value dims 0..511
@@ -48,24 +54,28 @@ constexpr int kSlotFlag = kSlotFac + 128 * 4;
 constexpr int kSlotBytes = kSlotFlag + 16;     // bytes moved per tile
 constexpr int kSlotStride = 17408;
 constexpr int kStatsBytes = 1024;              // l[128], m[128]
-constexpr int kQBoxBytes = 128 * 128;          // Q / O staging box: 128 rows x 128 bytes, 128B-swizzled
+constexpr int kQBoxBytes = 128 * 128;          // Q box: 128 rows x 128 bytes, 128B-swizzled
 constexpr int kQBytes = 9 * kQBoxBytes;        // Q [128 x 576] bf16
 // rank 0 layout
 constexpr int kOffK = 0;
-constexpr int kOffStage = kOffK + kKStages * kKStageBytes;
-constexpr int kEnd0 = kOffStage + 2 * kSlotStride;
+constexpr int kOffStage = kOffK + kKStages * kKStageBytes;  // two P staging buffers
+constexpr int kOffStatStage = kOffStage + 2 * kSlotStride;  // statistics staging
+constexpr int kEnd0 = kOffStatStage + kStatsBytes;
 // rank 1 layout
 constexpr int kOffV = 0;
 constexpr int kOffSlots = kOffV + kVStages * kVStageBytes;
-constexpr int kOffStats = kOffSlots + kSlots * kSlotStride;
-constexpr int kEnd1 = kOffStats + kStatsBytes;
+constexpr int kOffStats = kOffSlots + kSlots * kSlotStride;  // two statistics buffers
+constexpr int kEnd1 = kOffStats + 2 * kStatsBytes;
 constexpr int kSmem = (kEnd0 > kEnd1 ? kEnd0 : kEnd1) + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 288;                // rank 0: Q in columns 0..287, S buffers after it
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
+// warps that take work items from the scheduler: rank 0 MMA + producers + row warps, rank 1 also
+// the credit warp
+constexpr int kItemReaders0 = 1 + kProdWarps + 4, kItemReaders1 = kItemReaders0 + 1;
 static_assert(kColS + kSBufs * kKT <= kTmemCols, "rank 0 TMEM budget");
 static_assert(kQBytes <= kKStages * kKStageBytes, "Q is staged in rank 0's K ring");
-static_assert(8 * kQBoxBytes <= kVStages * kVStageBytes, "O is staged in rank 1's V ring, 8 boxes at a time");
+static_assert(kSmem <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -92,12 +102,21 @@ __device__ __forceinline__ int64_t latent_row(const AttnArgs& a, int t, int32_t 
   return r;
 }
 
+// A work item: tiles [tile0, tile0 + n_tiles) of token t's selection, written as key-split share
+// sp (t < 0: no more items).
+struct Item {
+  int t, sp, tile0, n_tiles;
+};
+
 struct Bars {
   // rank 0
-  uint64_t k_full[kKStages], k_empty[kKStages], s_full[kSBufs], s_empty[kSBufs], q_full, q_ready, p_empty[kSlots];
+  uint64_t k_full[kKStages], k_empty[kKStages], s_full[kSBufs], s_empty[kSBufs], q_full, q_ready, q_free;
+  uint64_t p_empty[kSlots], stats_empty[2];
   // rank 1
-  uint64_t v_full[kVStages], v_empty[kVStages], p_full[kSlots], ready[kSlots], slot_free[kSlots], stats_full;
-  uint64_t mma_done;
+  uint64_t v_full[kVStages], v_empty[kVStages], p_full[kSlots], ready[kSlots], slot_free[kSlots];
+  uint64_t stats_full[2], o_full, o_free;
+  // both
+  uint64_t sched_full[kSched], sched_empty[kSched], mma_done;
 };
 
 __device__ __forceinline__ uint32_t baddr(const uint64_t& b) { return ptx::smem_addr(&b); }
@@ -112,6 +131,42 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 // Warp-uniform bounded wait (all lanes agree on the outcome).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, const AttnArgs& a) {
   return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, a.status, a.limit_ns));
+}
+
+// Work item j of this warp's CTA, from the scheduler ring (the warp's lane 0 releases the slot).
+__device__ __forceinline__ bool read_item(Bars& bars, const Item* sched, int j, Item* it, volatile int* abort_flag,
+                                          const AttnArgs& a) {
+  const int slot = j % kSched;
+  if (!warp_wait(baddr(bars.sched_full[slot]), (j / kSched) & 1, abort_flag, a)) return false;
+  const volatile Item* e = sched + slot;
+  it->t = e->t;
+  it->sp = e->sp;
+  it->tile0 = e->tile0;
+  it->n_tiles = e->n_tiles;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(baddr(bars.sched_empty[slot]));
+  return true;
+}
+
+// First empty slot of a selection row (valid slots come first), by the whole warp: each round
+// probes 32 evenly spaced positions of the open interval, so k = 2048 takes three dependent loads.
+__device__ int first_empty_slot(const int32_t* idx_row, int k) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = k;  // every slot below lo is valid; the first empty one is in [lo, hi]
+  while (hi - lo > 32) {
+    const int step = (hi - lo + 31) / 32;
+    const int p = lo + lane * step;
+    const bool neg = p < hi && __ldg(idx_row + p) < 0;
+    const unsigned m = __ballot_sync(0xffffffffu, neg);
+    const int f = m ? __ffs(m) - 1 : 32;
+    if (f == 0) return lo;
+    const int nlo = lo + (f - 1) * step + 1;
+    hi = f < 32 ? lo + f * step : hi;
+    lo = nlo;
+  }
+  const int p = lo + lane;
+  const unsigned m = __ballot_sync(0xffffffffu, p < hi && __ldg(idx_row + p) < 0);
+  return m ? lo + __ffs(m) - 1 : hi;
 }
 
 // Gather of tile i: `nblk` 64-dim blocks (from latent dim 0) of each of the 64 selected rows into
@@ -145,34 +200,29 @@ __device__ __forceinline__ void gather_rows(const AttnArgs& a, int t, const int3
   }
 }
 
-// Producer loop shared by both ranks: ring of `stages` stages.  Completion of a stage is tracked
-// by the hardware (each producer thread's cp.async copies arrive on the stage's barrier when they
-// land), so producers never wait for their own copies and move straight on to the next stage.
-// The consumer issues fence.proxy.async after the barrier before the tensor core reads the stage.
+// One item's tiles through a producer ring of `stages` stages; g = tiles of earlier items.
+// Completion of a stage is tracked by the hardware (each producer thread's cp.async copies arrive
+// on the stage's barrier when they land), so producers never wait for their own copies.  The
+// consumer issues fence.proxy.async after the barrier before the tensor core reads the stage.
 template <int NBLK>
-__device__ __forceinline__ void producer_loop(const AttnArgs& a, int t, const int32_t* idx_row, int tile0, int n_tiles,
-                                              uint32_t ring, int stage_bytes, int stages,
-                                              uint64_t* full, uint64_t* empty, volatile int* abort_flag,
-                                              uint64_t* start) {
+__device__ __forceinline__ bool produce_item(const AttnArgs& a, const Item& it, int g, uint32_t ring, int stage_bytes,
+                                             int stages, uint64_t* full, uint64_t* empty, volatile int* abort_flag,
+                                             bool* range_err) {
   const int pw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
-  bool range_err = false;
-  if (n_tiles <= 0) return;
-  // rank 0's ring holds Q until it has been moved into tensor memory
-  if (start != nullptr && !warp_wait(baddr(*start), 0, abort_flag, a)) return;
+  const int32_t* idx_row = a.idx + static_cast<int64_t>(it.t) * a.k;
   // the first slot is valid whenever there is a tile (valid slots come first)
-  const int64_t fallback_row = latent_row(a, t, __ldg(idx_row), &range_err);
+  int64_t fallback_row = latent_row(a, it.t, __ldg(idx_row), range_err);
   if (fallback_row < 0) {  // first position out of range: nothing safe to substitute
     atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
+    fallback_row = 0;
   }
-  for (int i = 0; i < n_tiles; ++i) {
-    const int st = i % stages;
-    if (!warp_wait(baddr(empty[st]), ((i / stages) & 1) ^ 1, abort_flag, a)) break;
-    gather_rows<NBLK>(a, t, idx_row, tile0 + i, ring + st * stage_bytes, pw, lane,
-                      fallback_row < 0 ? 0 : fallback_row, &range_err);
+  for (int i = 0; i < it.n_tiles; ++i) {
+    const int gi = g + i, st = gi % stages;
+    if (!warp_wait(baddr(empty[st]), ((gi / stages) & 1) ^ 1, abort_flag, a)) return false;
+    gather_rows<NBLK>(a, it.t, idx_row, it.tile0 + i, ring + st * stage_bytes, pw, lane, fallback_row, range_err);
     ptx::cp_async_arrive_noinc(baddr(full[st]));
   }
-  ptx::cp_async_wait<0>();  // nothing of this thread's may still be in flight when the CTA exits
-  if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
+  return true;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -181,24 +231,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ Bars bars;
+  __shared__ Item sched[kSched];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag_s;
-  __shared__ int first_empty_s;
 
   const int rank = static_cast<int>(ptx::cluster_ctarank());
-  const int cl = blockIdx.x >> 1;
-  const int t = cl / a.n_split, sp = cl % a.n_split;
+  const int cl = blockIdx.x >> 1, n_cl = gridDim.x >> 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &abort_flag_s;
-  const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.k;
   const uint32_t sbase = ptx::smem_addr(smem);
-
-  // valid slots come first: the token's tile count follows from its first empty slot, found by
-  // every thread scanning a strided share of the row (the loads overlap the setup below)
-  int first_empty = a.k;
-#pragma unroll 4
-  for (int i = tid; i < a.k; i += kThreads)
-    if (__ldg(idx_row + i) < 0) first_empty = min(first_empty, i);
 
   if (tid == 0) {
     if (rank == 0) {
@@ -211,8 +252,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::mbar_init(baddr(bars.s_empty[b]), 128);
       }
       ptx::mbar_init(baddr(bars.q_full), 1);
-      ptx::mbar_init(baddr(bars.q_ready), 128);
+      ptx::mbar_init(baddr(bars.q_ready), kProducers);
+      ptx::mbar_init(baddr(bars.q_free), 1);
       for (int s = 0; s < kSlots; ++s) ptx::mbar_init(baddr(bars.p_empty[s]), 1);
+      for (int b = 0; b < 2; ++b) ptx::mbar_init(baddr(bars.stats_empty[b]), 1);
     } else {
       for (int s = 0; s < kVStages; ++s) {
         ptx::mbar_init(baddr(bars.v_full[s]), kProducers);
@@ -223,39 +266,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::mbar_init(baddr(bars.ready[s]), 128);
         ptx::mbar_init(baddr(bars.slot_free[s]), 1);
       }
-      ptx::mbar_init(baddr(bars.stats_full), 1);
+      for (int b = 0; b < 2; ++b) ptx::mbar_init(baddr(bars.stats_full[b]), 1);
+      ptx::mbar_init(baddr(bars.o_full), 1);
+      ptx::mbar_init(baddr(bars.o_free), 128);
+      // arm the first use of every P slot and statistics buffer for rank 0's bulk copies
+      for (int s = 0; s < kSlots; ++s) ptx::mbar_arrive_expect_tx(baddr(bars.p_full[s]), kSlotBytes);
+      for (int b = 0; b < 2; ++b) ptx::mbar_arrive_expect_tx(baddr(bars.stats_full[b]), kStatsBytes);
+    }
+    for (int s = 0; s < kSched; ++s) {
+      ptx::mbar_init(baddr(bars.sched_full[s]), 1);
+      ptx::mbar_init(baddr(bars.sched_empty[s]), rank == 0 ? kItemReaders0 : kItemReaders1);
     }
     ptx::mbar_init(baddr(bars.mma_done), 1);
     abort_flag_s = 0;
-    first_empty_s = a.k;
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
     ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
-  }
-  __syncthreads();
-  if (first_empty < a.k) atomicMin(&first_empty_s, first_empty);
-  __syncthreads();
-  // this cluster's share of the token's tiles
-  const int all_tiles = (first_empty_s + kKT - 1) / kKT;
-  const int per = (all_tiles + a.n_split - 1) / a.n_split;
-  const int tile0 = sp * per;
-  const int n_tiles = max(0, min(per, all_tiles - sp * per));
-  if (tid == 0 && n_tiles > 0) {
-    if (rank == 1) {
-      // arm the first use of every P slot and the final statistics for rank 0's bulk copies
-      for (int s = 0; s < kSlots; ++s) ptx::mbar_arrive_expect_tx(baddr(bars.p_full[s]), kSlotBytes);
-      ptx::mbar_arrive_expect_tx(baddr(bars.stats_full), kStatsBytes);
-    } else {
-      // Q [128 x 576] of the token -> the K ring, as nine 128B-swizzled [128 x 64] boxes (rows past
-      // the tensor read as zero; rows of the next token, when H < 128, are never used)
-      ptx::mbar_arrive_expect_tx(baddr(bars.q_full), kQBytes);
-#pragma unroll 1
-      for (int b = 0; b < 9; ++b)
-        ptx::tma_load_2d_hint(sbase + kOffK + b * kQBoxBytes, &qmap, baddr(bars.q_full), b * 64, t * a.H,
-                              ptx::l2_evict_first_policy());  // Q and O stream through: keep L2 for latent rows
-    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -263,19 +291,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (rank == 0) {
+  if (warp == kSchedWarp) {
+    // ================================================================ scheduler (both CTAs)
+    const int n_items = a.T * a.n_split;
+    for (int j = 0;; ++j) {
+      const int slot = j % kSched;
+      // the ring runs items ahead: this wait is never urgent, so it sleeps between polls
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait_sleep(baddr(bars.sched_empty[slot]), ((j / kSched) & 1) ^ 1,
+                                                        abort_flag, a.status, a.limit_ns, 1000)))
+        break;
+      const int id = cl + j * n_cl;
+      Item it{-1, 0, 0, 0};
+      if (id < n_items) {
+        it.t = id / a.n_split;
+        it.sp = id % a.n_split;
+        const int all_tiles = (first_empty_slot(a.idx + static_cast<int64_t>(it.t) * a.k, a.k) + kKT - 1) / kKT;
+        const int per = (all_tiles + a.n_split - 1) / a.n_split;
+        it.tile0 = it.sp * per;
+        it.n_tiles = max(0, min(per, all_tiles - it.sp * per));
+      }
+      if (lane == 0) {
+        volatile Item* e = sched + slot;
+        e->t = it.t;
+        e->sp = it.sp;
+        e->tile0 = it.tile0;
+        e->n_tiles = it.n_tiles;
+        ptx::mbar_arrive(baddr(bars.sched_full[slot]));
+      }
+      if (it.t < 0) break;
+    }
+  } else if (rank == 0) {
     // ================================================================ score CTA
     if (warp == 0) {
-      if (n_tiles > 0) {
-        // ---- S = Q K^T, issued by the whole warp (one elected lane)
-        constexpr uint32_t kIdescS = ptx::instr_desc(128, kKT, 1, 1, 0, 0);
-        bool ok = warp_wait(baddr(bars.q_ready), 0, abort_flag, a);
+      // ---- per item: Q -> ring (TMA), then S = Q K^T tile after tile, issued by the whole warp
+      constexpr uint32_t kIdescS = ptx::instr_desc(128, kKT, 1, 1, 0, 0);
+      int g = 0, nq = 0;
+      bool ok = true;
+      int q_last = -1;  // phase of the last Q load issued
+      for (int j = 0; ok; ++j) {
+        Item it;
+        if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
+        if (it.n_tiles == 0) continue;
+        // the ring and Q's TMEM columns are free once the previous item's products completed
+        if (nq > 0 && !warp_wait(baddr(bars.q_free), (nq - 1) & 1, abort_flag, a)) break;
+        if (lane == 0) {
+          // Q [128 x 576] of the token as nine 128B-swizzled [128 x 64] boxes (rows past the tensor
+          // read as zero; rows of the next token, when H < 128, are never used)
+          ptx::mbar_arrive_expect_tx(baddr(bars.q_full), kQBytes);
+#pragma unroll 1
+          for (int b = 0; b < 9; ++b)
+            ptx::tma_load_2d_hint(sbase + kOffK + b * kQBoxBytes, &qmap, baddr(bars.q_full), b * 64, it.t * a.H,
+                                  ptx::l2_evict_first_policy());  // Q and O stream: keep L2 for latent rows
+        }
+        __syncwarp();
+        q_last = nq;
+        if (!warp_wait(baddr(bars.q_ready), nq & 1, abort_flag, a)) break;
         ptx::tc_fence_after();
-        for (int i = 0; ok && i < n_tiles; ++i) {
-          const int st = i % kKStages, sb = i % kSBufs;
-          if (!warp_wait(baddr(bars.k_full[st]), (i / kKStages) & 1, abort_flag, a) ||
-              !warp_wait(baddr(bars.s_empty[sb]), ((i / kSBufs) & 1) ^ 1, abort_flag, a))
+        for (int i = 0; i < it.n_tiles; ++i) {
+          const int gi = g + i, st = gi % kKStages, sb = gi % kSBufs;
+          if (!warp_wait(baddr(bars.k_full[st]), (gi / kKStages) & 1, abort_flag, a) ||
+              !warp_wait(baddr(bars.s_empty[sb]), ((gi / kSBufs) & 1) ^ 1, abort_flag, a)) {
+            ok = false;
             break;
+          }
           ptx::fence_proxy_async_smem();  // gathered rows (generic-proxy writes) -> tensor-core reads
           ptx::tc_fence_after();
           const uint64_t db0 = ptx::smem_desc(sbase + kOffK + st * kKStageBytes, 16, 1024, ptx::kLayoutSw128);
@@ -287,22 +365,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::mma_commit_warp(baddr(bars.k_empty[st]));
           ptx::mma_commit_warp(baddr(bars.s_full[sb]));
         }
-        ptx::mma_commit_warp(baddr(bars.mma_done));
-        drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
+        ptx::mma_commit_warp(baddr(bars.q_free));
+        g += it.n_tiles;
+        ++nq;
       }
+      // after an abort, the last Q load may still be landing in the ring: let it finish
+      if (*abort_flag && q_last >= 0) drain_wait(baddr(bars.q_full), q_last & 1, a.limit_ns);
+      ptx::mma_commit_warp(baddr(bars.mma_done));
+      drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
     } else if (warp <= kProdWarps) {
-      producer_loop<9>(a, t, idx_row, tile0, n_tiles, sbase + kOffK, kKStageBytes, kKStages, bars.k_full, bars.k_empty,
-                       abort_flag, &bars.q_ready);
-    } else if (warp < kCreditWarp) {
-      // ------------------------------------------------------------ Q -> TMEM, then softmax
-      const int h = (warp & 3) * 32 + lane;
-      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      if (n_tiles > 0) {
+      // ---- per item: move Q from the ring into TMEM (three warps per lane quarter, three boxes
+      // each), then gather the item's K tiles
+      const int quarter = warp & 3, bsel = (warp - 1) >> 2;
+      const int h = quarter * 32 + lane;
+      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+      int g = 0, nq = 0;
+      bool range_err = false;
+      for (int j = 0;; ++j) {
+        Item it;
+        if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
+        if (it.n_tiles == 0) continue;
+        const bool got = warp_wait(baddr(bars.q_full), nq & 1, abort_flag, a);
         // row h of box b sits at b * 16 KB + h * 128 B with its 16-byte chunks XOR-swizzled by h & 7
-        const bool got = warp_wait(baddr(bars.q_full), 0, abort_flag, a);
         const uint8_t* qs = smem + kOffK + h * 128;
 #pragma unroll 1
-        for (int b = 0; b < 9; ++b) {
+        for (int b = bsel; b < 9; b += 3) {
           uint32_t v[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -315,130 +402,167 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(baddr(bars.q_ready));
+        // every producer has read Q out of the ring before any of them overwrites it
+        if (!got || !warp_wait(baddr(bars.q_ready), nq & 1, abort_flag, a)) break;
+        if (!produce_item<9>(a, it, g, sbase + kOffK, kKStageBytes, kKStages, bars.k_full, bars.k_empty, abort_flag,
+                             &range_err))
+          break;
+        g += it.n_tiles;
+        ++nq;
       }
+      ptx::cp_async_wait<0>();  // nothing of this thread's may still be in flight when the CTA exits
+      if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
+    } else if (warp < kCreditWarp) {
+      // ---- online softmax, one head row per thread
+      const int h = (warp & 3) * 32 + lane;
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t peer_slots = ptx::map_to_rank(sbase + kOffSlots, 1);
       uint8_t* stage = smem + kOffStage;
-      float m_used = -INFINITY, l = 0.f;
+      int g = 0, nq = 0;
       bool ok = true, range_err = false;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int sb = i % kSBufs;
-        // exits are taken by all 128 threads together (named barriers below are unbounded):
-        // a failed wait is voted on at the next barrier instead of breaking out alone
-        const bool got = warp_wait(baddr(bars.s_full[sb]), (i / kSBufs) & 1, abort_flag, a);
-        uint32_t s0[32], s1[32];
-        if (got) {
-          ptx::tc_fence_after();
-          ptx::tmem_ld32(tmem + kColS + sb * kKT + lane_base, s0);
-          ptx::tmem_ld32(tmem + kColS + sb * kKT + 32 + lane_base, s1);
-          ptx::tmem_wait_ld();
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(baddr(bars.s_empty[sb]));
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) s0[j] = s1[j] = 0;
-        }
-        // which of the 64 keys are real (empty / out-of-range slots are masked)
-        uint32_t vm[2];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int slot = (tile0 + i) * kKT + hh * 32 + lane;
-          const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
-          vm[hh] = __ballot_sync(0xffffffffu, latent_row(a, t, sidx, &range_err) >= 0);
-        }
-        float x[kKT];
-        float mt = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kKT; ++j) {
-          const uint32_t raw = j < 32 ? s0[j] : s1[j - 32];
-          x[j] = ((vm[j >> 5] >> (j & 31)) & 1u) ? __uint_as_float(raw) * a.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[j]);
-        }
-        const float m_new = fmaxf(m_used, mt);
-        const bool need = (i == 0) || (m_new > m_used + kRescaleThreshold);
-        const bool moved = __any_sync(0xffffffffu, need);
-        float fac = 1.f;
-        if (moved) {
-          fac = (i == 0) ? 0.f : fast_exp2(m_used - m_new);
-          l *= fac;
-          m_used = m_new;
-        }
-        float psum = 0.f;
-        uint32_t packed[kKT / 2];
-#pragma unroll
-        for (int j = 0; j < kKT; j += 2) {
-          const float p0 = fast_exp2(x[j] - m_used), p1 = fast_exp2(x[j + 1] - m_used);
-          psum += p0 + p1;
-          packed[j / 2] = pack_bf16(p0, p1);
-        }
-        l += psum;
-        // staging buffer i % 2 is free once the bulk copy of tile i - 2 has read it
-        const int sbuf = i & 1;
-        if (h == 0) ptx::bulk_wait_read<1>();
-        if (ptx::named_sync_or(1, 128, !got || *abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint8_t* sp = stage + sbuf * kSlotStride;
-        // P row h: 128 bytes = 8 chunks of 16 B, 128B swizzle (chunk c lands at c ^ (h & 7))
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(sp + h * 128 + ((c ^ (h & 7)) << 4)) =
-              make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-        reinterpret_cast<float*>(sp + kSlotFac)[h] = (moved && i > 0) ? fac : 1.f;
-        if (lane == 0) reinterpret_cast<int*>(sp + kSlotFlag)[warp & 3] = (moved && i > 0) ? 1 : 0;
-        ptx::fence_proxy_async_smem();
-        ptx::named_sync(2, 128);
-        if (h == 0) {
-          const int ps = i % kSlots;
-          if (!ptx::mbar_wait(baddr(bars.p_empty[ps]), ((i / kSlots) & 1) ^ 1, abort_flag, a.status, a.limit_ns)) {
-            ok = false;
+      for (int j = 0; ok; ++j) {
+        Item it;
+        if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
+        const int t = it.t;
+        const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.k;
+        float m_used = -INFINITY, l = 0.f;
+        for (int i = 0; i < it.n_tiles; ++i) {
+          const int gi = g + i, sb = gi % kSBufs;
+          // exits are taken by all 128 threads together (named barriers below are unbounded):
+          // a failed wait is voted on at the next barrier instead of breaking out alone
+          const bool got = warp_wait(baddr(bars.s_full[sb]), (gi / kSBufs) & 1, abort_flag, a);
+          uint32_t s0[32], s1[32];
+          if (got) {
+            ptx::tc_fence_after();
+            ptx::tmem_ld32(tmem + kColS + sb * kKT + lane_base, s0);
+            ptx::tmem_ld32(tmem + kColS + sb * kKT + 32 + lane_base, s1);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(baddr(bars.s_empty[sb]));
           } else {
-            ptx::bulk_copy_to_cluster(peer_slots + ps * kSlotStride, ptx::smem_addr(sp), kSlotBytes,
-                                      ptx::map_to_rank(baddr(bars.p_full[ps]), 1));
-            ptx::bulk_commit();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s0[e] = s1[e] = 0;
+          }
+          // which of the 64 keys are real (empty / out-of-range slots are masked)
+          uint32_t vm[2];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int slot = (it.tile0 + i) * kKT + hh * 32 + lane;
+            const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
+            vm[hh] = __ballot_sync(0xffffffffu, latent_row(a, t, sidx, &range_err) >= 0);
+          }
+          float x[kKT];
+          float mt = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < kKT; ++e) {
+            const uint32_t raw = e < 32 ? s0[e] : s1[e - 32];
+            x[e] = ((vm[e >> 5] >> (e & 31)) & 1u) ? __uint_as_float(raw) * a.scale_log2 : -INFINITY;
+            mt = fmaxf(mt, x[e]);
+          }
+          const float m_new = fmaxf(m_used, mt);
+          const bool need = (i == 0) || (m_new > m_used + kRescaleThreshold);
+          const bool moved = __any_sync(0xffffffffu, need);
+          float fac = 1.f;
+          if (moved) {
+            fac = (i == 0) ? 0.f : fast_exp2(m_used - m_new);
+            l *= fac;
+            m_used = m_new;
+          }
+          float psum = 0.f;
+          uint32_t packed[kKT / 2];
+#pragma unroll
+          for (int e = 0; e < kKT; e += 2) {
+            const float p0 = fast_exp2(x[e] - m_used), p1 = fast_exp2(x[e + 1] - m_used);
+            psum += p0 + p1;
+            packed[e / 2] = pack_bf16(p0, p1);
+          }
+          l += psum;
+          // staging buffer gi % 2 is free once the bulk copy of tile gi - 2 has read it
+          const int sbuf = gi & 1;
+          if (h == 0) ptx::bulk_wait_read<1>();
+          if (ptx::named_sync_or(1, 128, !got || *abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sp = stage + sbuf * kSlotStride;
+          // P row h: 128 bytes = 8 chunks of 16 B, 128B swizzle (chunk c lands at c ^ (h & 7))
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(sp + h * 128 + ((c ^ (h & 7)) << 4)) =
+                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+          reinterpret_cast<float*>(sp + kSlotFac)[h] = (moved && i > 0) ? fac : 1.f;
+          if (lane == 0) reinterpret_cast<int*>(sp + kSlotFlag)[warp & 3] = (moved && i > 0) ? 1 : 0;
+          ptx::fence_proxy_async_smem();
+          ptx::named_sync(2, 128);
+          // a failed wait here raises the abort flag, which the next vote picks up (`ok` stays
+          // uniform over the 128 threads)
+          if (h == 0) {
+            const int ps = gi % kSlots;
+            if (ptx::mbar_wait(baddr(bars.p_empty[ps]), ((gi / kSlots) & 1) ^ 1, abort_flag, a.status, a.limit_ns)) {
+              ptx::bulk_copy_to_cluster(peer_slots + ps * kSlotStride, ptx::smem_addr(sp), kSlotBytes,
+                                        ptx::map_to_rank(baddr(bars.p_full[ps]), 1));
+              ptx::bulk_commit();
+            }
           }
         }
+        if (it.n_tiles > 0) {
+          // the item's row statistics for rank 1's normalisation, into its buffer nq % 2
+          float* st = reinterpret_cast<float*>(smem + kOffStatStage);
+          if (h == 0) ptx::bulk_wait_read<0>();  // the previous statistics copy has read the staging
+          if (ptx::named_sync_or(1, 128, !ok || *abort_flag)) ok = false;
+          if (ok) {
+            st[h] = l;
+            st[128 + h] = m_used;
+            ptx::fence_proxy_async_smem();
+            ptx::named_sync(2, 128);
+            if (h == 0) {
+              const int b = nq & 1;
+              if (ptx::mbar_wait(baddr(bars.stats_empty[b]), ((nq >> 1) & 1) ^ 1, abort_flag, a.status,
+                                 a.limit_ns)) {
+                ptx::bulk_copy_to_cluster(ptx::map_to_rank(sbase + kOffStats + b * kStatsBytes, 1),
+                                          ptx::smem_addr(st), kStatsBytes,
+                                          ptx::map_to_rank(baddr(bars.stats_full[b]), 1));
+                ptx::bulk_commit();
+              }
+            }
+          }
+        }
+        const bool has = ok && it.n_tiles > 0;
+        if (a.n_split > 1) {
+          if (h < a.H) {
+            float* ml = a.part_ml + ((static_cast<int64_t>(t) * a.n_split + it.sp) * a.H + h) * 2;
+            ml[0] = has ? m_used : -INFINITY;
+            ml[1] = has ? l : 0.f;
+          }
+        } else if (a.lse != nullptr && h < a.H) {
+          a.lse[static_cast<int64_t>(t) * a.H + h] = has ? (m_used + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        }
+        g += it.n_tiles;
+        if (it.n_tiles > 0) ++nq;
       }
+      if (h == 0) ptx::bulk_wait_read<0>();  // no copy may still read this CTA's staging at exit
       if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
-      if (n_tiles > 0) {
-        // final row statistics for rank 1's normalisation
-        if (h == 0) ptx::bulk_wait_read<0>();
-        ptx::named_sync(1, 128);
-        float* st = reinterpret_cast<float*>(stage);
-        st[h] = l;
-        st[128 + h] = m_used;
-        ptx::fence_proxy_async_smem();
-        ptx::named_sync(2, 128);
-        if (h == 0 && ok) {
-          ptx::bulk_copy_to_cluster(ptx::map_to_rank(sbase + kOffStats, 1), ptx::smem_addr(stage), kStatsBytes,
-                                    ptx::map_to_rank(baddr(bars.stats_full), 1));
-          ptx::bulk_commit();
-        }
-        if (h == 0) ptx::bulk_wait_read<0>();
-      }
-      if (a.n_split > 1) {
-        if (h < a.H) {
-          float* ml = a.part_ml + ((static_cast<int64_t>(t) * a.n_split + sp) * a.H + h) * 2;
-          ml[0] = (ok && n_tiles > 0) ? m_used : -INFINITY;
-          ml[1] = (ok && n_tiles > 0) ? l : 0.f;
-        }
-      } else if (a.lse != nullptr && h < a.H) {
-        a.lse[static_cast<int64_t>(t) * a.H + h] =
-            (ok && n_tiles > 0) ? (m_used + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
-      }
     }
   } else {
     // ================================================================ value CTA
-    bool rescale_ok = true;
     if (warp == 0) {
-      if (n_tiles > 0) {
-        // ---- O += P V over two N = 256 halves, issued by the whole warp (one elected lane)
-        constexpr uint32_t kIdescPV = ptx::instr_desc(128, 256, 1, 1, 0, 1);
-        for (int i = 0; i < n_tiles; ++i) {
-          const int vs = i % kVStages, ps = i % kSlots;
-          if (!warp_wait(baddr(bars.v_full[vs]), (i / kVStages) & 1, abort_flag, a) ||
-              !warp_wait(baddr(bars.ready[ps]), (i / kSlots) & 1, abort_flag, a))
+      // ---- per item: O = sum of P V over its tiles (two N = 256 halves), issued by the whole warp
+      constexpr uint32_t kIdescPV = ptx::instr_desc(128, 256, 1, 1, 0, 1);
+      int g = 0, nq = 0;
+      bool ok = true;
+      for (int j = 0; ok; ++j) {
+        Item it;
+        if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
+        if (it.n_tiles == 0) continue;
+        // the previous item's O has been read out before this item's first product overwrites it
+        if (nq > 0 && !warp_wait(baddr(bars.o_free), (nq - 1) & 1, abort_flag, a)) break;
+        for (int i = 0; i < it.n_tiles; ++i) {
+          const int gi = g + i, vs = gi % kVStages, ps = gi % kSlots;
+          if (!warp_wait(baddr(bars.v_full[vs]), (gi / kVStages) & 1, abort_flag, a) ||
+              !warp_wait(baddr(bars.ready[ps]), (gi / kSlots) & 1, abort_flag, a)) {
+            ok = false;
             break;
+          }
           ptx::fence_proxy_async_smem();  // gathered rows (generic-proxy writes) -> tensor-core reads
           ptx::tc_fence_after();
           const uint32_t vst = sbase + kOffV + vs * kVStageBytes;
@@ -456,130 +580,150 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::mma_commit_warp(baddr(bars.v_empty[vs]));
           ptx::mma_commit_warp(baddr(bars.slot_free[ps]));
         }
-        ptx::mma_commit_warp(baddr(bars.mma_done));
-        drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
+        ptx::mma_commit_warp(baddr(bars.o_full));
+        g += it.n_tiles;
+        ++nq;
       }
+      ptx::mma_commit_warp(baddr(bars.mma_done));
+      drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
     } else if (warp <= kProdWarps) {
-      producer_loop<8>(a, t, idx_row, tile0, n_tiles, sbase + kOffV, kVStageBytes, kVStages, bars.v_full, bars.v_empty,
-                       abort_flag, nullptr);
+      int g = 0;
+      bool range_err = false;
+      for (int j = 0;; ++j) {
+        Item it;
+        if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
+        if (it.n_tiles == 0) continue;
+        if (!produce_item<8>(a, it, g, sbase + kOffV, kVStageBytes, kVStages, bars.v_full, bars.v_empty, abort_flag,
+                             &range_err))
+          break;
+        g += it.n_tiles;
+      }
+      ptx::cp_async_wait<0>();
+      if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
     } else if (warp < kCreditWarp) {
-      // ------------------------------------------------------------ rescale, then epilogue
+      // ---- per item: rescale O when rank 0 moved a row's max, then the epilogue: O / l in bf16
+      // (or, with a key split, the fp32 partial), one row per thread, straight from TMEM
       const int h = (warp & 3) * 32 + lane;
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint64_t policy = ptx::l2_evict_first_policy();  // written once, read by the next stage
+      int g = 0, nq = 0;
       bool ok = true;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int ps = i % kSlots;
-        if (!warp_wait(baddr(bars.p_full[ps]), (i / kSlots) & 1, abort_flag, a)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* sp = smem + kOffSlots + ps * kSlotStride;
-        if (reinterpret_cast<const volatile int*>(sp + kSlotFlag)[warp & 3]) {
-          // rank 0 moved this warp's running max: O must include PV(i-1) before it is rescaled
-          const int j = i - 1;
-          if (!warp_wait(baddr(bars.slot_free[j % kSlots]), (j / kSlots) & 1, abort_flag, a)) {
+      for (int j = 0; ok; ++j) {
+        Item it;
+        if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
+        for (int i = 0; ok && i < it.n_tiles; ++i) {
+          const int gi = g + i, ps = gi % kSlots;
+          if (!warp_wait(baddr(bars.p_full[ps]), (gi / kSlots) & 1, abort_flag, a)) {
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
-          const float f = reinterpret_cast<const float*>(sp + kSlotFac)[h];
+          const uint8_t* sp = smem + kOffSlots + ps * kSlotStride;
+          if (reinterpret_cast<const volatile int*>(sp + kSlotFlag)[warp & 3]) {
+            // rank 0 moved this warp's running max: O must include PV(gi - 1) before it is rescaled
+            const int pj = gi - 1;
+            if (!warp_wait(baddr(bars.slot_free[pj % kSlots]), (pj / kSlots) & 1, abort_flag, a)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const float f = reinterpret_cast<const float*>(sp + kSlotFac)[h];
 #pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
-            uint32_t o[32];
+            for (int c = 0; c < 16; ++c) {
+              uint32_t o[32];
+              ptx::tmem_ld32(tmem + lane_base + c * 32, o);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+              ptx::tmem_st32(tmem + lane_base + c * 32, o);
+            }
+            ptx::tmem_wait_st();
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(baddr(bars.ready[ps]));
+        }
+        // ---- epilogue of the item (the four warps decide together: named barriers are unbounded)
+        float inv_l = 0.f;
+        if (ok && it.n_tiles > 0) {
+          const int b = nq & 1;
+          ok = warp_wait(baddr(bars.o_full), nq & 1, abort_flag, a) &&
+               warp_wait(baddr(bars.stats_full[b]), (nq >> 1) & 1, abort_flag, a);
+          const float l = ok ? reinterpret_cast<const float*>(smem + kOffStats + b * kStatsBytes)[h] : 0.f;
+          inv_l = l > 0.f ? 1.f / l : 0.f;
+        }
+        if (ptx::named_sync_or(1, 128, !ok)) ok = false;
+        if (ok && it.n_tiles > 0 && h == 0) {
+          // the statistics buffer is free again: arm its next use and tell rank 0
+          const int b = nq & 1;
+          ptx::mbar_arrive_expect_tx(baddr(bars.stats_full[b]), kStatsBytes);
+          ptx::mbar_arrive_cluster(ptx::map_to_rank(baddr(bars.stats_empty[b]), 0));
+        }
+        ptx::tc_fence_after();
+        const bool split = a.n_split > 1;
+        const int64_t orow = split ? (static_cast<int64_t>(it.t) * a.n_split + it.sp) * a.H + h
+                                   : static_cast<int64_t>(it.t) * a.H + h;
+        const bool has = ok && it.n_tiles > 0;
+#pragma unroll 1
+        for (int c = 0; c < 16; ++c) {
+          uint32_t o[32];
+          if (has) {
             ptx::tmem_ld32(tmem + lane_base + c * 32, o);
             ptx::tmem_wait_ld();
+          } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            ptx::tmem_st32(tmem + lane_base + c * 32, o);
+            for (int e = 0; e < 32; ++e) o[e] = 0u;  // an item without keys (or a failed one) writes zeros
           }
-          ptx::tmem_wait_st();
-        }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(baddr(bars.ready[ps]));
-      }
-      rescale_ok = ok;
-    } else if (lane == 0) {
-      // ------------------------------------------------------------ slot credits back to rank 0
-      for (int i = 0; i < n_tiles; ++i) {
-        const int ps = i % kSlots;
-        if (!ptx::mbar_wait(baddr(bars.slot_free[ps]), (i / kSlots) & 1, abort_flag, a.status, a.limit_ns)) break;
-        if (i + kSlots < n_tiles) {
-          ptx::mbar_arrive_expect_tx(baddr(bars.p_full[ps]), kSlotBytes);
-          ptx::mbar_arrive_cluster(ptx::map_to_rank(baddr(bars.p_empty[ps]), 0));
-        }
-      }
-    }
-    if (warp >= 1 && warp < kCreditWarp) {
-      // ---- epilogue, by warps 1..16 (four per TMEM lane quarter, each with a quarter of the
-      // columns): O / l is staged as 128B-swizzled [128 x 128 B] boxes in the drained V ring (a
-      // thread writes its own row, conflict-free), then copied out row-contiguously with 16-byte
-      // stores: bf16 out (8 boxes of 64 columns) or, with a key split, the fp32 partial (16 boxes
-      // of 32 columns, in two rounds of 8).  The rescale warps first wait for the last PV product
-      // and the final statistics; a failure anywhere is voted on at the barrier.
-      const int quarter = warp & 3, grp = (warp - 1) >> 2;
-      const int h = quarter * 32 + lane;
-      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-      bool bad = false;
-      if (warp >= kRowWarp0 && n_tiles > 0) {
-        const int j = n_tiles - 1;
-        bad = !rescale_ok || !ptx::mbar_wait(baddr(bars.stats_full), 0, abort_flag, a.status, a.limit_ns) ||
-              !ptx::mbar_wait(baddr(bars.slot_free[j % kSlots]), (j / kSlots) & 1, abort_flag, a.status, a.limit_ns);
-      }
-      bad = ptx::named_sync_or(1, 512, bad);
-      const bool has_rows = !bad && n_tiles > 0;
-      const float l = has_rows ? reinterpret_cast<const float*>(smem + kOffStats)[h] : 0.f;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      ptx::tc_fence_after();
-      const bool split = a.n_split > 1;
-      const int64_t out_row0 = split ? (static_cast<int64_t>(t) * a.n_split + sp) * a.H : static_cast<int64_t>(t) * a.H;
-      const int row_bytes = split ? kDV * 4 : kDV * 2;
-      uint8_t* gout = split ? reinterpret_cast<uint8_t*>(a.part_o) : reinterpret_cast<uint8_t*>(a.out);
-      gout += out_row0 * row_bytes;
-      const uint64_t policy = ptx::l2_evict_first_policy();  // written once, read by the next stage
-      uint8_t* stage_row = smem + kOffV + h * 128;
-      const int per = split ? 2 : 4;  // 32-column blocks per warp and round
-#pragma unroll 1
-      for (int round = 0; round < (split ? 2 : 1); ++round) {
-#pragma unroll 1
-        for (int k = 0; k < per; ++k) {
-          const int cr = grp * per + k;  // block within the round
-          const int c = round * 8 + cr;  // 32-column block of O
-          uint32_t o[32];
-          ptx::tmem_ld32(tmem + lane_base + c * 32, o);
-          ptx::tmem_wait_ld();
-          if (h < a.H) {
-            if (split) {
-              uint8_t* box = stage_row + cr * kQBoxBytes;
+          if (h >= a.H) continue;
+          if (split) {
+            uint8_t* dst = reinterpret_cast<uint8_t*>(a.part_o + orow * kDV + c * 32);
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<float4*>(box + ((e ^ (h & 7)) << 4)) =
-                    make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
-                                __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l);
-            } else {
-              uint8_t* box = stage_row + (c >> 1) * kQBoxBytes;
+            for (int e = 0; e < 8; ++e)
+              ptx::st_global_v4_hint(dst + 16 * e,
+                                     make_uint4(__float_as_uint(__uint_as_float(o[4 * e]) * inv_l),
+                                                __float_as_uint(__uint_as_float(o[4 * e + 1]) * inv_l),
+                                                __float_as_uint(__uint_as_float(o[4 * e + 2]) * inv_l),
+                                                __float_as_uint(__uint_as_float(o[4 * e + 3]) * inv_l)),
+                                     policy);
+          } else {
+            uint8_t* dst = reinterpret_cast<uint8_t*>(a.out + orow * kDV + c * 32);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int chunk = (c & 1) * 4 + e;
-                uint4 pk;
-                pk.x = pack_bf16(__uint_as_float(o[8 * e]) * inv_l, __uint_as_float(o[8 * e + 1]) * inv_l);
-                pk.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv_l, __uint_as_float(o[8 * e + 3]) * inv_l);
-                pk.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv_l, __uint_as_float(o[8 * e + 5]) * inv_l);
-                pk.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv_l, __uint_as_float(o[8 * e + 7]) * inv_l);
-                *reinterpret_cast<uint4*>(box + ((chunk ^ (h & 7)) << 4)) = pk;
-              }
+            for (int e = 0; e < 4; ++e)
+              ptx::st_global_v4_hint(
+                  dst + 16 * e,
+                  make_uint4(pack_bf16(__uint_as_float(o[8 * e]) * inv_l, __uint_as_float(o[8 * e + 1]) * inv_l),
+                             pack_bf16(__uint_as_float(o[8 * e + 2]) * inv_l, __uint_as_float(o[8 * e + 3]) * inv_l),
+                             pack_bf16(__uint_as_float(o[8 * e + 4]) * inv_l, __uint_as_float(o[8 * e + 5]) * inv_l),
+                             pack_bf16(__uint_as_float(o[8 * e + 6]) * inv_l, __uint_as_float(o[8 * e + 7]) * inv_l)),
+                  policy);
+          }
+        }
+        if (it.n_tiles > 0) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(baddr(bars.o_free));  // O has been read: the next item may overwrite it
+          g += it.n_tiles;
+          ++nq;
+        }
+      }
+    } else if (warp == kCreditWarp) {
+      // ---- slot credits back to rank 0: slot ps is re-armed for tile gi + kSlots once tile gi's
+      // products completed (a re-armed slot that no tile reaches is never waited on)
+      int g = 0;
+      bool ok = true;
+      for (int j = 0; ok; ++j) {
+        Item it;
+        if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
+        if (lane == 0) {
+          for (int i = 0; i < it.n_tiles; ++i) {
+            const int gi = g + i, ps = gi % kSlots;
+            if (!ptx::mbar_wait(baddr(bars.slot_free[ps]), (gi / kSlots) & 1, abort_flag, a.status, a.limit_ns)) {
+              ok = false;
+              break;
             }
+            ptx::mbar_arrive_expect_tx(baddr(bars.p_full[ps]), kSlotBytes);
+            ptx::mbar_arrive_cluster(ptx::map_to_rank(baddr(bars.p_empty[ps]), 0));
           }
         }
-        ptx::named_sync(1, 512);
-        // this round's 1024 bytes of each row: chunk q = (row q / 64, 16-byte chunk q % 64)
-#pragma unroll 4
-        for (int q = (warp - 1) * 32 + lane; q < a.H * 64; q += 512) {
-          const int row = q >> 6, cc = q & 63, cb = cc & 7;
-          const uint4 v = *reinterpret_cast<const uint4*>(smem + kOffV + (cc >> 3) * kQBoxBytes + row * 128 +
-                                                          ((cb ^ (row & 7)) << 4));
-          ptx::st_global_v4_hint(gout + static_cast<int64_t>(row) * row_bytes + round * 1024 + cc * 16, v, policy);
-        }
-        ptx::named_sync(1, 512);  // the staging boxes are free again
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        g += it.n_tiles;
       }
     }
   }
@@ -633,7 +777,12 @@ cudaError_t launch_sparse_attn(const AttnArgs& a0, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<dim3(2 * a.T * a.n_split), kThreads, kSmem, stream>>>(a, qmap);
+  // one cluster per SM pair, each taking every n_clusters-th work item
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t items = static_cast<int64_t>(a.T) * a.n_split;
+  const int clusters = static_cast<int>(items < sms / 2 ? items : sms / 2);
+  sparse_attn_kernel<<<dim3(2 * clusters), kThreads, kSmem, stream>>>(a, qmap);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_split == 1) return e;
   return launch_attn_combine(a, stream);
