@@ -200,6 +200,29 @@ __device__ __forceinline__ void gather_rows(const AttnArgs& a, int t, const int3
   }
 }
 
+// Transpose of N x N 16-byte chunks among N consecutive lanes: lane i's v[k] (chunk k of its
+// row) becomes chunk i of lane k's row, so that N lanes then store one row's N chunks together.
+template <int N>
+__device__ __forceinline__ void transpose_chunks(uint4 (&v)[N]) {
+  const int i = threadIdx.x & (N - 1);
+#pragma unroll
+  for (int sh = N / 2; sh >= 1; sh >>= 1) {
+    const bool up = (i & sh) != 0;
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      if (k & sh) continue;
+      const uint4 send = up ? v[k] : v[k ^ sh];
+      uint4 recv;
+      recv.x = __shfl_xor_sync(0xffffffffu, send.x, sh);
+      recv.y = __shfl_xor_sync(0xffffffffu, send.y, sh);
+      recv.z = __shfl_xor_sync(0xffffffffu, send.z, sh);
+      recv.w = __shfl_xor_sync(0xffffffffu, send.w, sh);
+      if (up) v[k] = recv;
+      else v[k ^ sh] = recv;
+    }
+  }
+}
+
 // One item's tiles through a producer ring of `stages` stages; g = tiles of earlier items.
 // Completion of a stage is tracked by the hardware (each producer thread's cp.async copies arrive
 // on the stage's barrier when they land), so producers never wait for their own copies.  The
@@ -658,10 +681,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_cluster(ptx::map_to_rank(baddr(bars.stats_empty[b]), 0));
         }
         ptx::tc_fence_after();
+        // Each 32-column block of O is transposed among groups of lanes so that a store instruction
+        // writes whole row segments: bf16 rows (64 bytes per block) by 4 lanes, fp32 partial rows
+        // (128 bytes) by 8 lanes.
         const bool split = a.n_split > 1;
-        const int64_t orow = split ? (static_cast<int64_t>(it.t) * a.n_split + it.sp) * a.H + h
-                                   : static_cast<int64_t>(it.t) * a.H + h;
         const bool has = ok && it.n_tiles > 0;
+        const int64_t row0 = split ? (static_cast<int64_t>(it.t) * a.n_split + it.sp) * a.H : static_cast<int64_t>(it.t) * a.H;
+        const int wrow = (warp & 3) * 32;  // this warp's first head row
 #pragma unroll 1
         for (int c = 0; c < 16; ++c) {
           uint32_t o[32];
@@ -672,28 +698,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = 0u;  // an item without keys (or a failed one) writes zeros
           }
-          if (h >= a.H) continue;
           if (split) {
-            uint8_t* dst = reinterpret_cast<uint8_t*>(a.part_o + orow * kDV + c * 32);
+            uint4 v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              ptx::st_global_v4_hint(dst + 16 * e,
-                                     make_uint4(__float_as_uint(__uint_as_float(o[4 * e]) * inv_l),
-                                                __float_as_uint(__uint_as_float(o[4 * e + 1]) * inv_l),
-                                                __float_as_uint(__uint_as_float(o[4 * e + 2]) * inv_l),
-                                                __float_as_uint(__uint_as_float(o[4 * e + 3]) * inv_l)),
-                                     policy);
+              v[e] = make_uint4(__float_as_uint(__uint_as_float(o[4 * e]) * inv_l),
+                                __float_as_uint(__uint_as_float(o[4 * e + 1]) * inv_l),
+                                __float_as_uint(__uint_as_float(o[4 * e + 2]) * inv_l),
+                                __float_as_uint(__uint_as_float(o[4 * e + 3]) * inv_l));
+            transpose_chunks<8>(v);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int hr = wrow + (lane & ~7) + k;
+              if (hr < a.H)
+                ptx::st_global_v4_hint(a.part_o + (row0 + hr) * kDV + c * 32 + (lane & 7) * 4, v[k], policy);
+            }
           } else {
-            uint8_t* dst = reinterpret_cast<uint8_t*>(a.out + orow * kDV + c * 32);
+            uint4 v[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              ptx::st_global_v4_hint(
-                  dst + 16 * e,
-                  make_uint4(pack_bf16(__uint_as_float(o[8 * e]) * inv_l, __uint_as_float(o[8 * e + 1]) * inv_l),
-                             pack_bf16(__uint_as_float(o[8 * e + 2]) * inv_l, __uint_as_float(o[8 * e + 3]) * inv_l),
-                             pack_bf16(__uint_as_float(o[8 * e + 4]) * inv_l, __uint_as_float(o[8 * e + 5]) * inv_l),
-                             pack_bf16(__uint_as_float(o[8 * e + 6]) * inv_l, __uint_as_float(o[8 * e + 7]) * inv_l)),
-                  policy);
+              v[e] = make_uint4(pack_bf16(__uint_as_float(o[8 * e]) * inv_l, __uint_as_float(o[8 * e + 1]) * inv_l),
+                                pack_bf16(__uint_as_float(o[8 * e + 2]) * inv_l, __uint_as_float(o[8 * e + 3]) * inv_l),
+                                pack_bf16(__uint_as_float(o[8 * e + 4]) * inv_l, __uint_as_float(o[8 * e + 5]) * inv_l),
+                                pack_bf16(__uint_as_float(o[8 * e + 6]) * inv_l, __uint_as_float(o[8 * e + 7]) * inv_l));
+            transpose_chunks<4>(v);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int hr = wrow + (lane & ~3) + k;
+              if (hr < a.H)
+                ptx::st_global_v4_hint(a.out + (row0 + hr) * kDV + c * 32 + (lane & 3) * 8, v[k], policy);
+            }
           }
         }
         if (it.n_tiles > 0) {
