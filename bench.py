@@ -423,8 +423,9 @@ def bench_decode(dsa, synth, args, peaks, cid=5):
 
 
 def bench_e2e(dsa, d, cfg, args):
-    """Same prefill step through dsa_forward with inputs and output in pinned host memory:
-    per step H2D of every input, the forward, and D2H of the attention output."""
+    """The prefill step with inputs and output in pinned host memory, through dsa_prefill_host (the
+    library's host-buffer entry point): every step copies every input in and the attention output
+    back, chunk by chunk, overlapped with the kernels."""
     names = ["q8", "q_scale", "w", "k8", "k_scale", "q", "kv"]
     need = sum(d[n].numel() * d[n].element_size() for n in names) + cfg.L * cfg.H * 512 * 2
     try:
@@ -436,24 +437,16 @@ def bench_e2e(dsa, d, cfg, args):
     host = {n: torch.empty_like(d[n], device="cpu").pin_memory() for n in names}
     for n in names:
         host[n].copy_(d[n])
-    host_out = torch.empty((cfg.L, cfg.H, 512), dtype=torch.bfloat16).pin_memory()
-    dev = {n: torch.empty_like(d[n]) for n in names}
-    f = dsa.Forward.prefill(dev, cfg.k, cfg.scale, chunk_rows=args.chunk)
+    f = dsa.PrefillHost(host, cfg.k, cfg.scale, chunk_rows=args.e2e_chunk)
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = host_out.numel() * 2
+    d2h = f.out.numel() * 2
 
-    def step():
-        for n in names:
-            dev[n].copy_(host[n], non_blocking=True)
-        f()
-        host_out.copy_(f.out, non_blocking=True)
-
-    step()
+    f()
     torch.cuda.synchronize()
     n_steps = max(2, min(args.steps, 3))
     a = _rec()
     for _ in range(n_steps):
-        step()
+        f()
     b = _rec()
     b.synchronize()
     ms = a.elapsed_time(b) / n_steps
@@ -462,7 +455,7 @@ def bench_e2e(dsa, d, cfg, args):
         raise RuntimeError(f"e2e status {st}")
     return {"value": round(cfg.L / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 2),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_steps,
-            "path": "dsa_forward (C ABI) with pinned host buffers"}
+            "path": f"dsa_prefill_host (C ABI), pinned host buffers, {args.e2e_chunk}-row chunks"}
 
 
 # ------------------------------------------------------------------------------------ oracle arm
@@ -550,6 +543,7 @@ def main():
     p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k", "prefill128k_tail", "decode", "decode32k"],
                    help="the others run single pieces (used for profiler captures)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--e2e-chunk", type=int, default=2048, help="query rows per chunk of the host-buffer pipeline")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-decode", action="store_true")

@@ -223,6 +223,26 @@ dsa_status_t dsa_forward(const dsa_forward_args* args, void* ws, size_t ws_bytes
                          dsa_stream_t stream);
 
 /*
+ * dsa_prefill_host — the prefill forward (mode DSA_MODE_PREFILL of dsa_forward) with every
+ * tensor in HOST memory: args->q8, q_scale, w, k8, k_scale, q, kv and the outputs out, lse
+ * (or NULL) and idx (or NULL) are host pointers, laid out as for dsa_forward.  The keys are
+ * copied to the device once; then the query rows move in chunks of chunk_rows (0 = library
+ * choice) through two device slots, so that one chunk's copies in and out run while the other
+ * chunk's kernels run (the same kernels as dsa_forward, the same results).  Copies are
+ * asynchronous only from page-locked (pinned) host memory; pageable memory works but
+ * serialises them.
+ * `ws` is a caller-owned device buffer of at least dsa_prefill_host_workspace_size(args) bytes,
+ * 256-byte aligned.  The call only enqueues work: the kernels run on `stream` and the copies on
+ * two streams the library keeps per device, ordered after the work already on `stream`; the
+ * outputs are in host memory once `stream` reaches the point after this call (synchronise it
+ * before reading them, and do not touch the host buffers before then).  Errors as dsa_forward;
+ * a failed copy or event returns DSA_ERR_CUDA.
+ */
+size_t dsa_prefill_host_workspace_size(const dsa_forward_args* args);
+dsa_status_t dsa_prefill_host(const dsa_forward_args* args, void* ws, size_t ws_bytes,
+                              dsa_stream_t stream);
+
+/*
  * dsa_device_status — synchronises `stream`, then returns and clears the status word
  * the kernels write on the current device (DSA_OK if nothing was recorded).
  * Returns DSA_ERR_CUDA if the synchronisation itself fails.

@@ -24,7 +24,7 @@ MODE_PREFILL, MODE_DECODE = 0, 1
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_index", "dsa_index_paged", "dsa_topk", "dsa_sparse_attn",
            "dsa_forward_workspace_size", "dsa_forward", "dsa_device_status", "dsa_selftest_wait_timeout",
            "dsa_decode_noalloc", "dsa_decode_noalloc_capacity", "dsa_sparse_attn_split_workspace_size",
-           "dsa_sparse_attn_split")
+           "dsa_sparse_attn_split", "dsa_prefill_host_workspace_size", "dsa_prefill_host")
 
 
 class DSAError(RuntimeError):
@@ -73,6 +73,8 @@ def _load():
         "dsa_decode_noalloc_capacity": ([], ctypes.c_size_t),
         "dsa_sparse_attn_split_workspace_size": ([I, I, I], ctypes.c_size_t),
         "dsa_sparse_attn_split": ([P, P, I64, P, I64, I, P, I, I, I, F, P, P, I, P, ctypes.c_size_t, P], I),
+        "dsa_prefill_host_workspace_size": ([ctypes.POINTER(ForwardArgs)], ctypes.c_size_t),
+        "dsa_prefill_host": ([ctypes.POINTER(ForwardArgs), P, ctypes.c_size_t, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -254,6 +256,44 @@ class Forward:
     def __call__(self, stream=None):
         s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(self.out)
         _check(lib.dsa_forward(ctypes.byref(self.args), _ptr(self.ws), self.ws.numel(), s), "dsa_forward")
+        return self.out
+
+
+class PrefillHost:
+    """Prefill forward with inputs and outputs in host memory (dsa_prefill_host): owns the device workspace.
+
+    PrefillHost(inputs, k, scale) with inputs = dict(q8, q_scale, w, k8, k_scale, q, kv) as CPU tensors
+    (pinned for overlapped copies); calling it enqueues the chunked pipeline on the current stream of
+    `device`; the outputs (self.out, and self.lse / self.idx if given) are valid after that stream is
+    synchronised.
+    """
+
+    def __init__(self, inp, k, scale, q_pos0=0, chunk_rows=0, out=None, lse=None, idx=None, device="cuda"):
+        q8 = inp["q8"]
+        for n, t in inp.items():
+            if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+                raise TypeError(f"{n}: expected a contiguous CPU tensor")
+        T, H_I, _ = q8.shape
+        H = inp["q"].shape[1]
+        pin = q8.is_pinned()
+        self.out = torch.empty((T, H, 512), dtype=torch.bfloat16, pin_memory=pin) if out is None else out
+        self.lse, self.idx = lse, idx
+        self.args = ForwardArgs(mode=MODE_PREFILL, H_I=H_I, H=H, k=k, scale=scale, T=T, S=inp["k8"].shape[0],
+                                q_pos0=q_pos0, chunk_rows=chunk_rows,
+                                q8=_ptr(q8), q_scale=_ptr(inp["q_scale"]), w=_ptr(inp["w"]), k8=_ptr(inp["k8"]),
+                                k_scale=_ptr(inp["k_scale"]), q=_ptr(inp["q"]), kv=_ptr(inp["kv"]),
+                                out=_ptr(self.out), lse=_ptr(lse), idx=_ptr(idx))
+        self._keep = inp
+        n = lib.dsa_prefill_host_workspace_size(ctypes.byref(self.args))
+        if n == 0:
+            raise DSAError(1, "dsa_prefill_host_workspace_size")
+        self.device = torch.device(device)
+        self.ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+
+    def __call__(self, stream=None):
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        _check(lib.dsa_prefill_host(ctypes.byref(self.args), _ptr(self.ws), self.ws.numel(),
+                                    ctypes.c_void_p(s.cuda_stream)), "dsa_prefill_host")
         return self.out
 
 

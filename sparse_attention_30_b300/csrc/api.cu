@@ -194,6 +194,51 @@ dsa_status_t plan_forward(const dsa_forward_args* a, FwdPlan* p) {
   return DSA_OK;
 }
 
+// Device workspace of dsa_prefill_host: the keys once, then two slots of query-row chunk inputs
+// and outputs (so that the copies of one chunk overlap the kernels of the other), and one score
+// block.
+struct HostPlan {
+  FwdPlan f;
+  size_t k8, k_scale, kv;                  // keys
+  size_t q8, q_scale, w, q, idx, out, lse; // one slot (chunk rows)
+  size_t slot, scores, total;
+};
+
+dsa_status_t plan_prefill_host(const dsa_forward_args* a, HostPlan* h) {
+  if (!a || a->mode != DSA_MODE_PREFILL) return DSA_ERR_INVALID_ARG;
+  dsa_status_t st = plan_forward(a, &h->f);
+  if (st != DSA_OK) return st;
+  const size_t C = static_cast<size_t>(h->f.chunk), S = static_cast<size_t>(a->S);
+  h->k8 = align256(S * 128);
+  h->k_scale = align256(S * 4);
+  h->kv = align256(S * 576 * 2);
+  h->q8 = align256(C * a->H_I * 128);
+  h->q_scale = align256(C * a->H_I * 4);
+  h->w = align256(C * a->H_I * 4);
+  h->q = align256(C * a->H * 576 * 2);
+  h->idx = align256(C * a->k * 4);
+  h->out = align256(C * a->H * 512 * 2);
+  h->lse = align256(C * a->H * 4);
+  h->slot = h->q8 + h->q_scale + h->w + h->q + h->idx + h->out + h->lse;
+  h->scores = h->f.scores_bytes;
+  h->total = h->k8 + h->k_scale + h->kv + 2 * h->slot + h->scores;
+  return DSA_OK;
+}
+
+// Two non-blocking streams per device for the host pipeline's copies (created on first use).
+bool copy_streams(cudaStream_t* in, cudaStream_t* out) {
+  static cudaStream_t s_in[kMaxDevices], s_out[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!s_in[dev] && (cudaStreamCreateWithFlags(&s_in[dev], cudaStreamNonBlocking) != cudaSuccess ||
+                     cudaStreamCreateWithFlags(&s_out[dev], cudaStreamNonBlocking) != cudaSuccess))
+    return false;
+  *in = s_in[dev];
+  *out = s_out[dev];
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -361,6 +406,106 @@ dsa_status_t dsa_forward(const dsa_forward_args* a, void* ws, size_t ws_bytes, d
                            a->B, a->H, a->k, a->scale, a->out, a->lse, p.n_split,
                            p.n_split > 1 ? reinterpret_cast<float*>(part) : nullptr,
                            p.n_split > 1 ? reinterpret_cast<float*>(part + p.part_o_bytes) : nullptr, s);
+}
+
+size_t dsa_prefill_host_workspace_size(const dsa_forward_args* args) {
+  HostPlan h;
+  if (plan_prefill_host(args, &h) != DSA_OK) return 0;
+  return h.total;
+}
+
+dsa_status_t dsa_prefill_host(const dsa_forward_args* a, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  HostPlan hp;
+  dsa_status_t st = plan_prefill_host(a, &hp);
+  if (st != DSA_OK) return st;
+  if (!a->q8 || !a->q_scale || !a->w || !a->k8 || !a->k_scale || !a->q || !a->kv || !a->out)
+    return DSA_ERR_INVALID_ARG;
+  if (a->T == 0) return DSA_OK;
+  if (!ws || ws_bytes < hp.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
+  const int C = hp.f.chunk, H_I = a->H_I, H = a->H, K = a->k;
+  char* p = static_cast<char*>(ws);
+  uint8_t* k8 = reinterpret_cast<uint8_t*>(p);
+  float* k_scale = reinterpret_cast<float*>(p + hp.k8);
+  uint16_t* kv = reinterpret_cast<uint16_t*>(p + hp.k8 + hp.k_scale);
+  char* slots = p + hp.k8 + hp.k_scale + hp.kv;
+  float* scores = reinterpret_cast<float*>(slots + 2 * hp.slot);
+  struct Slot {
+    uint8_t* q8; float* q_scale; float* w; uint16_t* q; int32_t* idx; uint16_t* out; float* lse;
+  } sl[2];
+  for (int b = 0; b < 2; ++b) {
+    char* c = slots + b * hp.slot;
+    sl[b].q8 = reinterpret_cast<uint8_t*>(c);
+    sl[b].q_scale = reinterpret_cast<float*>(c += hp.q8);
+    sl[b].w = reinterpret_cast<float*>(c += hp.q_scale);
+    sl[b].q = reinterpret_cast<uint16_t*>(c += hp.w);
+    sl[b].idx = reinterpret_cast<int32_t*>(c += hp.q);
+    sl[b].out = reinterpret_cast<uint16_t*>(c += hp.idx);
+    sl[b].lse = reinterpret_cast<float*>(c += hp.out);
+  }
+  cudaStream_t s_in, s_out, s = stream;
+  if (!copy_streams(&s_in, &s_out)) return DSA_ERR_CUDA;
+  // events: start (the workspace is free of earlier work on `stream`), keys copied, and per slot:
+  // inputs copied, kernels done, outputs copied
+  cudaEvent_t ev[8];
+  for (int i = 0; i < 8; ++i)
+    if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+      return DSA_ERR_CUDA;
+    }
+  cudaEvent_t start = ev[0], keys = ev[1], in_done[2] = {ev[2], ev[3]}, comp_done[2] = {ev[4], ev[5]},
+              out_done[2] = {ev[6], ev[7]};
+  auto H2D = cudaMemcpyHostToDevice;
+  auto D2H = cudaMemcpyDeviceToHost;
+  bool ok = cudaEventRecord(start, s) == cudaSuccess && cudaStreamWaitEvent(s_in, start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(s_out, start, 0) == cudaSuccess &&
+            cudaMemcpyAsync(k8, a->k8, static_cast<size_t>(a->S) * 128, H2D, s_in) == cudaSuccess &&
+            cudaMemcpyAsync(k_scale, a->k_scale, static_cast<size_t>(a->S) * 4, H2D, s_in) == cudaSuccess &&
+            cudaMemcpyAsync(kv, a->kv, static_cast<size_t>(a->S) * 576 * 2, H2D, s_in) == cudaSuccess &&
+            cudaEventRecord(keys, s_in) == cudaSuccess && cudaStreamWaitEvent(s, keys, 0) == cudaSuccess;
+  const int n_chunks = (a->T + C - 1) / C;
+  for (int c = 0; ok && c < n_chunks; ++c) {
+    const int b = c & 1, r0 = c * C, rows = std::min(C, a->T - r0);
+    const Slot& q = sl[b];
+    // inputs of chunk c into slot b, once chunk c - 2's kernels are done with it
+    if (c >= 2) ok = ok && cudaStreamWaitEvent(s_in, comp_done[b], 0) == cudaSuccess;
+    ok = ok &&
+         cudaMemcpyAsync(q.q8, a->q8 + static_cast<size_t>(r0) * H_I * 128, static_cast<size_t>(rows) * H_I * 128, H2D,
+                         s_in) == cudaSuccess &&
+         cudaMemcpyAsync(q.q_scale, a->q_scale + static_cast<size_t>(r0) * H_I, static_cast<size_t>(rows) * H_I * 4,
+                         H2D, s_in) == cudaSuccess &&
+         cudaMemcpyAsync(q.w, a->w + static_cast<size_t>(r0) * H_I, static_cast<size_t>(rows) * H_I * 4, H2D, s_in) ==
+             cudaSuccess &&
+         cudaMemcpyAsync(q.q, a->q + static_cast<size_t>(r0) * H * 576, static_cast<size_t>(rows) * H * 576 * 2, H2D,
+                         s_in) == cudaSuccess &&
+         cudaEventRecord(in_done[b], s_in) == cudaSuccess;
+    if (!ok) break;
+    // kernels of chunk c on the caller's stream, once its inputs landed and chunk c - 2's outputs left
+    ok = cudaStreamWaitEvent(s, in_done[b], 0) == cudaSuccess &&
+         (c < 2 || cudaStreamWaitEvent(s, out_done[b], 0) == cudaSuccess);
+    if (!ok) break;
+    const int64_t pos0 = a->q_pos0 + r0;
+    st = dsa_index(q.q8, q.q_scale, q.w, k8, k_scale, rows, a->S, H_I, pos0, scores, hp.f.ld, s);
+    if (st == DSA_OK) st = dsa_topk(scores, hp.f.ld, rows, nullptr, a->S, pos0, K, q.idx, s);
+    if (st == DSA_OK) st = dsa_sparse_attn(q.q, kv, a->S, nullptr, 0, 0, q.idx, rows, H, K, a->scale, q.out, q.lse, s);
+    if (st != DSA_OK) break;
+    ok = cudaEventRecord(comp_done[b], s) == cudaSuccess;
+    // outputs of chunk c back to the host
+    ok = ok && cudaStreamWaitEvent(s_out, comp_done[b], 0) == cudaSuccess &&
+         cudaMemcpyAsync(a->out + static_cast<size_t>(r0) * H * 512, q.out, static_cast<size_t>(rows) * H * 512 * 2,
+                         D2H, s_out) == cudaSuccess &&
+         (!a->lse || cudaMemcpyAsync(a->lse + static_cast<size_t>(r0) * H, q.lse, static_cast<size_t>(rows) * H * 4,
+                                     D2H, s_out) == cudaSuccess) &&
+         (!a->idx || cudaMemcpyAsync(a->idx + static_cast<size_t>(r0) * K, q.idx, static_cast<size_t>(rows) * K * 4,
+                                     D2H, s_out) == cudaSuccess) &&
+         cudaEventRecord(out_done[b], s_out) == cudaSuccess;
+  }
+  // the caller's stream covers the whole call: it waits for the last copies out
+  if (ok) {
+    for (int b = 0; b < 2 && b < n_chunks; ++b) ok = ok && cudaStreamWaitEvent(s, out_done[b], 0) == cudaSuccess;
+  }
+  for (int i = 0; i < 8; ++i) cudaEventDestroy(ev[i]);  // released once their work completes
+  if (st != DSA_OK) return st;
+  return ok ? DSA_OK : DSA_ERR_CUDA;
 }
 
 dsa_status_t dsa_device_status(dsa_stream_t stream) {

@@ -126,6 +126,27 @@ def test_forward_workspace_and_validation():
     assert dsa.lib.dsa_forward(ctypes.byref(d), None, 0, None) == 1
 
 
+def test_prefill_host_workspace_and_validation():
+    dsa = _lib()
+    a = dsa.ForwardArgs(mode=dsa.MODE_PREFILL, H_I=64, H=128, k=2048, scale=0.07, T=4096, S=4096, q_pos0=0,
+                        chunk_rows=1024)
+    n = dsa.lib.dsa_prefill_host_workspace_size(ctypes.byref(a))
+    keys = 4096 * 128 + 4096 * 4 + 4096 * 576 * 2
+    slot = 1024 * (64 * 128 + 64 * 4 + 64 * 4 + 128 * 576 * 2 + 2048 * 4 + 128 * 512 * 2 + 128 * 4)
+    assert n == keys + 2 * slot + 1024 * 4096 * 4
+    a.mode = dsa.MODE_DECODE                          # prefill only
+    assert dsa.lib.dsa_prefill_host_workspace_size(ctypes.byref(a)) == 0
+    assert dsa.lib.dsa_prefill_host(ctypes.byref(a), None, 0, None) == 1
+    a.mode = dsa.MODE_PREFILL
+    assert dsa.lib.dsa_prefill_host(ctypes.byref(a), None, 0, None) == 1       # null inputs
+    buf = ctypes.create_string_buffer(64)
+    P = ctypes.cast(buf, ctypes.c_void_p).value
+    for f in ("q8", "q_scale", "w", "k8", "k_scale", "q", "kv", "out"):
+        setattr(a, f, P)
+    assert dsa.lib.dsa_prefill_host(ctypes.byref(a), None, 0, None) == 3       # no workspace
+    assert dsa.lib.dsa_prefill_host(ctypes.byref(a), P + 1, n, None) == 3      # misaligned / too small
+
+
 def test_forward_args_layout_matches_c():
     dsa = _lib()
     fields = [f for f, _ in dsa.ForwardArgs._fields_]

@@ -342,6 +342,26 @@ def test_forward_prefill_config2_sampled_rows(dsa):
     assert swaps <= len(rows)  # near-tie swaps are rare
 
 
+def test_prefill_host_matches_device_forward(dsa):
+    # the host-buffer pipeline (ragged 1000-row chunks through two device slots) gives the device
+    # forward's outputs: the same selected sets (the order of a selection is not fixed, and the
+    # attention sums in selection order, so outputs agree to rounding)
+    cfg = synth.config(2)
+    hinp = synth.prefill_inputs(cfg)
+    f = _run_prefill(dsa, _cuda(hinp), cfg, chunk_rows=1000)
+    host = {n: t.contiguous().pin_memory() for n, t in hinp.items()}
+    lse = torch.empty((cfg.L, cfg.H), dtype=torch.float32).pin_memory()
+    idx = torch.empty((cfg.L, cfg.k), dtype=torch.int32).pin_memory()
+    g = dsa.PrefillHost(host, cfg.k, cfg.scale, chunk_rows=1000, lse=lse, idx=idx)
+    for _ in range(2):  # twice: the second call reuses the slots and events
+        g()
+        torch.cuda.synchronize()
+        assert dsa.device_status() == 0
+        assert torch.equal(torch.sort(idx, dim=1).values, torch.sort(f.idx.cpu(), dim=1).values)
+        assert (g.out.float() - f.out.float().cpu()).abs().max().item() <= 1e-2
+        assert (lse - f.lse.cpu()).abs().max().item() <= 1e-4
+
+
 @pytest.mark.parametrize("cid", [3, 5])
 def test_forward_decode_full_config(dsa, cid):
     cfg = synth.config(cid)
