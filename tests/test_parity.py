@@ -358,7 +358,8 @@ def test_prefill_host_matches_device_forward(dsa):
         torch.cuda.synchronize()
         assert dsa.device_status() == 0
         assert torch.equal(torch.sort(idx, dim=1).values, torch.sort(f.idx.cpu(), dim=1).values)
-        assert (g.out.float() - f.out.float().cpu()).abs().max().item() <= 1e-2
+        diff = (g.out.float() - f.out.float().cpu()).abs()
+        assert diff.max().item() <= MAX_TOL and diff.mean().item() <= 1e-4  # a bf16 ulp where the order differs
         assert (lse - f.lse.cpu()).abs().max().item() <= 1e-4
 
 
