@@ -272,8 +272,8 @@ def run_ours(args, dist, rank, ws):
     # DRAM bytes (read + write) per query row from the ncu capture of the 1024-row 128K tail
     # (profiles/prefill128k_tail_full.md), scaled to the launch's rows; the capture starts from a
     # flushed L2, so it overstates the steady state a little.  None where no capture matches.
-    traffic_per_row = {"sparse_attn": (0.422053e9 + 0.1166912e9) / 1024, "indexer": (0.063149e9 + 0.475974e9) / 1024,
-                       "topk": (1.053748e9 + 0.007288e9) / 1024}
+    traffic_per_row = {"sparse_attn": (0.424813e9 + 0.116605e9) / 1024, "indexer": (0.063544e9 + 0.475494e9) / 1024,
+                       "topk": (1.015358e9 + 0.007002e9) / 1024}
     traffic = traffic_per_row.get(dom_name)
     if traffic is not None:
         traffic = round(traffic * cfg.L / kern[dom_name]["launches"])
