@@ -19,6 +19,9 @@ address; sections are the pages' own numbering):
       (same page, §2.1.2 output equation), MQA mode of MLA: one latent row
       c_s per token shared by every query head (same page, §2.2).  The value
       is the first 512 dims of the 576-dim latent, softmax scale 1/sqrt(192).
+  * dense causal attention over every row s <= t: the computation DSA replaces,
+      which vpshk.cn/20260227158.html and 10100.com/article/43188788 §1 compare
+      DSA's cost against.
 
 Every step is the plain definition: exact decode of the FP8 / bf16 inputs to
 float64, dot products in float64 (exact for FP8 inputs), a stable full sort for
@@ -30,6 +33,6 @@ brute-force enumeration and closed forms.
 """
 from .dsa import (  # noqa: F401
     e4m3_to_f64, bf16_bits_to_f64, indexer_row, indexer_scores, topk_row, topk_rows,
-    attention_row, prefill_row, prefill_rows, decode_row, decode_gather,
+    attention_row, dense_causal_row, prefill_row, prefill_rows, decode_row, decode_gather,
     selected_pairs, causal_pairs, index_sets_match, attention_error,
 )

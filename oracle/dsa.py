@@ -145,6 +145,18 @@ def attention_row(q_t, latent_rows, scale: float, d_value: int = 512):
     return o, (m + np.log(l))[:, 0]
 
 
+def dense_causal_row(q_t, kv, pos: int, scale: float, d_value: int = 512):
+    """Dense causal attention of one token at absolute position `pos` over every latent row
+    0..pos: the MQA-mode MLA computation that DSA replaces.
+
+    vpshk.cn/20260227158.html (the dense V3.1 model's cost grows with the text, V3.2's stays
+    nearly flat) and 10100.com/article/43188788 §1 ("actual effect": about half the long-context
+    cost of the dense model) compare against it; it is DSA with every preceding row selected
+    (k >= pos + 1).  Returns (o [H, d_value], lse [H]) like attention_row.
+    """
+    return attention_row(q_t, _as_np(kv)[: pos + 1], scale, d_value)
+
+
 # ----------------------------------------------------------------------------
 # Whole forward, one query row at a time
 # ----------------------------------------------------------------------------

@@ -188,6 +188,21 @@ def test_dense_limit_equals_causal_sdpa_config1():
         np.testing.assert_allclose(r["o"], ref[t], rtol=1e-12, atol=1e-12)
 
 
+def test_dense_causal_row_equals_causal_sdpa_with_offset():
+    # rows of a chunk that starts at absolute position q_pos0 see keys 0 .. q_pos0 + i
+    g = torch.Generator().manual_seed(11)
+    H, S, q_pos0, T = 6, 300, 170, 130
+    q = torch.randn(T, H, 576, generator=g).to(torch.bfloat16)
+    kv = torch.randn(S, 576, generator=g).to(torch.bfloat16)
+    mask = torch.arange(S)[None, :] <= (q_pos0 + torch.arange(T))[:, None]
+    ref = _sdpa_f64(q, kv, mask=mask[None, None], scale=0.05)
+    for i in [0, 1, 63, 64, 129]:
+        o, lse = oracle.dense_causal_row(q[i], kv, q_pos0 + i, 0.05)
+        np.testing.assert_allclose(o, ref[i], rtol=1e-12, atol=1e-12)
+        logits = 0.05 * (q[i].double() @ kv[: q_pos0 + i + 1].double().T)
+        np.testing.assert_allclose(lse, torch.logsumexp(logits, dim=1).numpy(), rtol=1e-13)
+
+
 def test_sparse_attention_equals_masked_sdpa():
     cfg = synth.config(1)
     inp = synth.prefill_inputs(cfg)
