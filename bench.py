@@ -221,6 +221,8 @@ def run_ours(args, dist, rank, ws):
                 "data": "synthetic", "config": {"workload": res["workload"]}, "decode": res}
     if args.workload == "prefill128k_tail":
         return bench_prefill_tail(dsa, synth, args, peaks)
+    if args.workload == "dense_curve":
+        return bench_dense_curve(dsa, synth, args, peaks)
     cid = {"prefill128k": 4, "prefill4k": 2}[args.workload]
     cfg = synth.config(cid)
     if rank:
@@ -349,6 +351,55 @@ def bench_prefill_tail(dsa, synth, args, peaks, n_rows=1024):
             "higher_is_better": True, "dtype": "fp8-e4m3 / bf16", "data": "synthetic",
             "config": {"workload": f"prefill L={cfg.L}: query rows {r0}..{cfg.L - 1}, k=2048, H=128, H_I=64"},
             "kernels_ms": kms}
+
+
+def bench_dense_curve(dsa, synth, args, peaks, lengths=(4096, 16384, 32768, 65536, 131072)):
+    """Prefill time of one sequence against its length, DSA (indexer -> top-k -> sparse attention)
+    beside dense causal MLA attention over the same Q / latent rows: the cost-versus-length
+    comparison of the pages (dense cost grows with L^2, DSA's attention with k L)."""
+    curve = []
+    for L in lengths:
+        cfg = synth.config(4, L=L)
+        d = synth.prefill_inputs(cfg, device="cuda")
+        runner = PrefillRunner(dsa, d, cfg, min(args.chunk, L))
+        out = torch.empty((L, cfg.H, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((L, cfg.H), dtype=torch.float32, device="cuda")
+
+        def dense():
+            dsa.dense_causal_attn(d["q"], d["kv"], cfg.scale, out=out, lse=lse)
+
+        res = {"L": L}
+        for name, fn in (("dsa", runner.step), ("dense", dense)):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            n = args.steps if L <= 32768 else max(2, min(args.steps, 3))
+            a = _rec()
+            for _ in range(n):
+                fn()
+            b = _rec()
+            b.synchronize()
+            res[f"{name}_ms"] = round(a.elapsed_time(b) / n, 3)
+        st = dsa.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at L={L}")
+        dense_flop = 2.0 * cfg.H * (576 + 512) * L * (L + 1) / 2
+        res["dense_tflops"] = round(dense_flop / (res["dense_ms"] * 1e-3) / 1e12, 1)
+        res["dense_frac"] = round(res["dense_tflops"] / peaks["bf16_sus"], 4)
+        res["dsa_tok_s"] = round(L / (res["dsa_ms"] * 1e-3), 1)
+        res["dense_tok_s"] = round(L / (res["dense_ms"] * 1e-3), 1)
+        res["dense_over_dsa"] = round(res["dense_ms"] / res["dsa_ms"], 3)
+        curve.append(res)
+        del d, runner, out, lse
+        torch.cuda.empty_cache()
+    last = curve[-1]
+    return {"metric": "prefill tokens/s, DSA vs dense causal MLA attention, against sequence length",
+            "value": last["dsa_tok_s"], "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": last["dsa_ms"], "higher_is_better": True,
+            "dtype": "fp8-e4m3 indexer / bf16 attention (fp32 accum)", "data": "synthetic",
+            "config": {"workload": "one prefill sequence per L (128K recipe), H=128, k=2048, H_I=64",
+                       "dense": "dsa_dense_causal_attn over the same Q and latent rows (no indexer, no top-k)"},
+            "curve": curve}
 
 
 def bench_decode(dsa, synth, args, peaks, cid=5):
@@ -540,7 +591,8 @@ def main():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--chunk", type=int, default=8192)
-    p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k", "prefill128k_tail", "decode", "decode32k"],
+    p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k", "prefill128k_tail", "decode", "decode32k",
+                                                       "dense_curve"],
                    help="the others run single pieces (used for profiler captures)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--e2e-chunk", type=int, default=2048, help="query rows per chunk of the host-buffer pipeline")

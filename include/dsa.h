@@ -160,6 +160,31 @@ dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_
                                    uint16_t* out, float* lse, int n_split, void* ws, size_t ws_bytes,
                                    dsa_stream_t stream);
 
+/*
+ * dsa_dense_causal_attn — dense causal attention in the same MQA mode of MLA: every row attends
+ * to every latent row at or before its own position.  This is the computation DSA replaces
+ * (vpshk.cn/20260227158.html: the dense V3.1 model's cost climbs with the text length while
+ * V3.2's stays nearly flat; 10100.com/article/43188788 §1: about half the long-context cost),
+ * provided as the baseline DSA is measured against.  It equals dsa_sparse_attn with the
+ * selection {0, ..., q_pos0 + t} for row t.
+ *
+ * For every row t (absolute position q_pos0 + t) and head h:
+ *     o[t,h,:] = sum_{s = 0 .. q_pos0 + t} softmax_s(scale * q[t,h,:] . c_s) * c_s[0:512]
+ *
+ *   q   [T, H, 576] bf16, 16-byte aligned, 1 <= H <= 128
+ *   kv  [n_kv_rows, 576] bf16 latent rows of positions 0 .. n_kv_rows - 1, 16-byte aligned;
+ *       q_pos0 >= 0, q_pos0 + T <= n_kv_rows < 2^31
+ *   out [T, H, 512] bf16, 16-byte aligned
+ *   lse [T, H] fp32 natural-log sum-exp of the scaled logits, or NULL
+ * Same arithmetic as dsa_sparse_attn (bf16 tensor-core products, fp32 accumulation and softmax);
+ * the latent rows are read as contiguous 64-row tiles.  Errors: DSA_ERR_INVALID_ARG /
+ * DSA_ERR_UNSUPPORTED before any launch; DSA_ERR_CUDA if the launch fails; device timeouts in the
+ * status word (dsa_device_status).
+ */
+dsa_status_t dsa_dense_causal_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, int T, int H,
+                                   int64_t q_pos0, float scale, uint16_t* out, float* lse,
+                                   dsa_stream_t stream);
+
 /* Forward modes. */
 enum { DSA_MODE_PREFILL = 0, DSA_MODE_DECODE = 1 };
 

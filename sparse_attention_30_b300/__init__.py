@@ -24,7 +24,8 @@ MODE_PREFILL, MODE_DECODE = 0, 1
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_index", "dsa_index_paged", "dsa_topk", "dsa_sparse_attn",
            "dsa_forward_workspace_size", "dsa_forward", "dsa_device_status", "dsa_selftest_wait_timeout",
            "dsa_decode_noalloc", "dsa_decode_noalloc_capacity", "dsa_sparse_attn_split_workspace_size",
-           "dsa_sparse_attn_split", "dsa_prefill_host_workspace_size", "dsa_prefill_host")
+           "dsa_sparse_attn_split", "dsa_prefill_host_workspace_size", "dsa_prefill_host",
+           "dsa_dense_causal_attn")
 
 
 class DSAError(RuntimeError):
@@ -72,6 +73,7 @@ def _load():
         "dsa_decode_noalloc": ([ctypes.POINTER(ForwardArgs), P], I),
         "dsa_decode_noalloc_capacity": ([], ctypes.c_size_t),
         "dsa_sparse_attn_split_workspace_size": ([I, I, I], ctypes.c_size_t),
+        "dsa_dense_causal_attn": ([P, P, I64, I, I, I64, F, P, P, P], I),
         "dsa_sparse_attn_split": ([P, P, I64, P, I64, I, P, I, I, I, F, P, P, I, P, ctypes.c_size_t, P], I),
         "dsa_prefill_host_workspace_size": ([ctypes.POINTER(ForwardArgs)], ctypes.c_size_t),
         "dsa_prefill_host": ([ctypes.POINTER(ForwardArgs), P, ctypes.c_size_t, P], I),
@@ -178,6 +180,22 @@ def sparse_attn(q, kv, idx, scale, block_table=None, page_size=0, out=None, lse=
     bt_stride = block_table.stride(0) if block_table is not None else 0
     _check(lib.dsa_sparse_attn(_ptr(q), _ptr(kv), n_rows, _ptr(block_table), bt_stride, page_size, _ptr(idx), T, H,
                                k, float(scale), _ptr(out), _ptr(lse), _stream(q)), "dsa_sparse_attn")
+    return out, lse
+
+
+def dense_causal_attn(q, kv, scale, q_pos0=0, out=None, lse=None, want_lse=True):
+    """Dense causal attention over every latent row up to each row's position (dsa_dense_causal_attn):
+    the dense MLA baseline.  q [T, H, 576] holds rows at positions q_pos0 .. q_pos0 + T - 1, kv [S, 576].
+    Returns (out [T,H,512] bf16, lse [T,H] | None)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv, torch.bfloat16, "kv", 2)
+    T, H, _ = q.shape
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    _check(lib.dsa_dense_causal_attn(_ptr(q), _ptr(kv), kv.shape[0], T, H, int(q_pos0), float(scale), _ptr(out),
+                                     _ptr(lse), _stream(q)), "dsa_dense_causal_attn")
     return out, lse
 
 

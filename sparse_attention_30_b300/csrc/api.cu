@@ -357,6 +357,23 @@ extern "C" dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, i
                            nullptr, nullptr, stream);
 }
 
+extern "C" dsa_status_t dsa_dense_causal_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, int T, int H,
+                                              int64_t q_pos0, float scale, uint16_t* out, float* lse,
+                                              dsa_stream_t stream) {
+  if (T < 0 || H < 1 || q_pos0 < 0 || n_kv_rows < 1 || n_kv_rows > INT32_MAX) return DSA_ERR_INVALID_ARG;
+  if (q_pos0 + static_cast<int64_t>(T) > n_kv_rows) return DSA_ERR_INVALID_ARG;
+  if (!q || !kv || !out || !aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+  if (H > 128) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  int* status = status_ptr();
+  if (!status) return DSA_ERR_CUDA;
+  AttnArgs a{};
+  a.q = q; a.kv = kv; a.n_kv_rows = n_kv_rows; a.idx = nullptr; a.T = T; a.H = H; a.k = 0; a.q_pos0 = q_pos0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = out; a.lse = lse; a.status = status; a.limit_ns = kWaitLimitNs; a.n_split = 1;
+  return from_cuda(launch_sparse_attn(a, stream));
+}
+
 size_t dsa_forward_workspace_size(const dsa_forward_args* args) {
   FwdPlan p;
   if (plan_forward(args, &p) != DSA_OK) return 0;

@@ -70,8 +70,9 @@ struct AttnArgs {
   const int32_t* block_table; // NULL: contiguous
   int64_t bt_stride;
   int page_size;
-  const int32_t* idx;         // [T, k]
+  const int32_t* idx;         // [T, k]; NULL selects the dense causal mode
   int T, H, k;
+  int64_t q_pos0;             // dense causal mode (idx NULL): row t attends latent rows 0 .. q_pos0 + t
   float scale_log2;           // softmax scale * log2(e)
   uint16_t* out;              // [T, H, 512] bf16
   float* lse;                 // [T, H] or NULL

@@ -192,7 +192,8 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
 }
 
 // 2-D tiled TMA load into shared memory, completing on an mbarrier.  x (the innermost
-// coordinate) is always 0 here, so it meets the 16-byte alignment rule.
+// coordinate) times the element size must be a multiple of 16 bytes: every caller passes 0 or a
+// multiple of 64 elements.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                            int x, int y) {
   asm volatile(

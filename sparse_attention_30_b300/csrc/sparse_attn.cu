@@ -248,8 +248,43 @@ __device__ __forceinline__ bool produce_item(const AttnArgs& a, const Item& it, 
   return true;
 }
 
+// Dense causal mode: tile i of an item covers the 64 consecutive latent rows from
+// (tile0 + i) * 64, so lane 0 of one warp moves it with NBLK tensor-map box loads ([64 rows x 64
+// dims] each, 128B-swizzled, the same layout the gathers write); rows past the tensor read as zero
+// and the softmax masks every key after the token's own position.  *issued counts the tiles whose
+// loads were started, for the drain after an abort.
+template <int NBLK>
+__device__ __forceinline__ bool produce_item_dense(const AttnArgs& a, const CUtensorMap* kvmap, const Item& it, int g,
+                                                   uint32_t ring, int stage_bytes, int stages, uint64_t* full,
+                                                   uint64_t* empty, volatile int* abort_flag, int* issued) {
+  for (int i = 0; i < it.n_tiles; ++i) {
+    const int gi = g + i, st = gi % stages;
+    if (!warp_wait(baddr(empty[st]), ((gi / stages) & 1) ^ 1, abort_flag, a)) return false;
+    if ((threadIdx.x & 31) == 0) {
+      ptx::mbar_arrive_expect_tx(baddr(full[st]), NBLK * kBlockBytes);
+#pragma unroll 1
+      for (int b = 0; b < NBLK; ++b)
+        ptx::tma_load_2d(ring + st * stage_bytes + b * kBlockBytes, kvmap, baddr(full[st]), b * 64,
+                         (it.tile0 + i) * kKT);
+    }
+    __syncwarp();
+    *issued = gi + 1;
+  }
+  return true;
+}
+
+// After an abort, the tensor-map loads of the last `stages` tiles may still be landing in the ring:
+// wait (bounded) until they have, so that no copy writes into the CTA's shared memory after exit.
+__device__ __forceinline__ void drain_dense(uint64_t* full, int stages, int issued, uint64_t limit_ns) {
+  for (int gi = issued > stages ? issued - stages : 0; gi < issued; ++gi)
+    drain_wait(baddr(full[gi % stages]), (gi / stages) & 1, limit_ns);
+}
+
+// kDense: dense causal mode (no selection; row t attends latent rows 0 .. q_pos0 + t).
+template <bool kDense>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
+    sparse_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap kvmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -263,11 +298,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &abort_flag_s;
   const uint32_t sbase = ptx::smem_addr(smem);
+  constexpr bool dense = kDense;
+  const uint32_t fill = dense ? 1u : static_cast<uint32_t>(kProducers);  // arrivals per ring stage
 
   if (tid == 0) {
     if (rank == 0) {
       for (int s = 0; s < kKStages; ++s) {
-        ptx::mbar_init(baddr(bars.k_full[s]), kProducers);
+        ptx::mbar_init(baddr(bars.k_full[s]), fill);
         ptx::mbar_init(baddr(bars.k_empty[s]), 1);
       }
       for (int b = 0; b < kSBufs; ++b) {
@@ -281,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int b = 0; b < 2; ++b) ptx::mbar_init(baddr(bars.stats_empty[b]), 1);
     } else {
       for (int s = 0; s < kVStages; ++s) {
-        ptx::mbar_init(baddr(bars.v_full[s]), kProducers);
+        ptx::mbar_init(baddr(bars.v_full[s]), fill);
         ptx::mbar_init(baddr(bars.v_empty[s]), 1);
       }
       for (int s = 0; s < kSlots; ++s) {
@@ -328,7 +365,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (id < n_items) {
         it.t = id / a.n_split;
         it.sp = id % a.n_split;
-        const int all_tiles = (first_empty_slot(a.idx + static_cast<int64_t>(it.t) * a.k, a.k) + kKT - 1) / kKT;
+        const int64_t n_keys = dense ? a.q_pos0 + it.t + 1 : first_empty_slot(a.idx + static_cast<int64_t>(it.t) * a.k, a.k);
+        const int all_tiles = static_cast<int>((n_keys + kKT - 1) / kKT);
         const int per = (all_tiles + a.n_split - 1) / a.n_split;
         it.tile0 = it.sp * per;
         it.n_tiles = max(0, min(per, all_tiles - it.sp * per));
@@ -402,7 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int quarter = warp & 3, bsel = (warp - 1) >> 2;
       const int h = quarter * 32 + lane;
       const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-      int g = 0, nq = 0;
+      int g = 0, nq = 0, issued = 0;
       bool range_err = false;
       for (int j = 0;; ++j) {
         Item it;
@@ -427,12 +465,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(baddr(bars.q_ready));
         // every producer has read Q out of the ring before any of them overwrites it
         if (!got || !warp_wait(baddr(bars.q_ready), nq & 1, abort_flag, a)) break;
-        if (!produce_item<9>(a, it, g, sbase + kOffK, kKStageBytes, kKStages, bars.k_full, bars.k_empty, abort_flag,
-                             &range_err))
+        if constexpr (dense) {
+          if (warp == 1 && !produce_item_dense<9>(a, &kvmap, it, g, sbase + kOffK, kKStageBytes, kKStages, bars.k_full,
+                                                  bars.k_empty, abort_flag, &issued))
+            break;
+        } else if (!produce_item<9>(a, it, g, sbase + kOffK, kKStageBytes, kKStages, bars.k_full, bars.k_empty,
+                                    abort_flag, &range_err)) {
           break;
+        }
         g += it.n_tiles;
         ++nq;
       }
+      if (dense && warp == 1 && *abort_flag) drain_dense(bars.k_full, kKStages, issued, a.limit_ns);
       ptx::cp_async_wait<0>();  // nothing of this thread's may still be in flight when the CTA exits
       if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
     } else if (warp < kCreditWarp) {
@@ -447,7 +491,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         Item it;
         if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
         const int t = it.t;
-        const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.k;
+        const int32_t* idx_row = dense ? nullptr : a.idx + static_cast<int64_t>(t) * a.k;
         float m_used = -INFINITY, l = 0.f;
         for (int i = 0; i < it.n_tiles; ++i) {
           const int gi = g + i, sb = gi % kSBufs;
@@ -471,8 +515,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int slot = (it.tile0 + i) * kKT + hh * 32 + lane;
-            const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
-            vm[hh] = __ballot_sync(0xffffffffu, latent_row(a, t, sidx, &range_err) >= 0);
+            if constexpr (dense) {
+              vm[hh] = __ballot_sync(0xffffffffu, slot <= a.q_pos0 + t);
+            } else {
+              const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
+              vm[hh] = __ballot_sync(0xffffffffu, latent_row(a, t, sidx, &range_err) >= 0);
+            }
           }
           float x[kKT];
           float mt = -INFINITY;
@@ -610,17 +658,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mma_commit_warp(baddr(bars.mma_done));
       drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
     } else if (warp <= kProdWarps) {
-      int g = 0;
+      int g = 0, issued = 0;
       bool range_err = false;
       for (int j = 0;; ++j) {
         Item it;
         if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
         if (it.n_tiles == 0) continue;
-        if (!produce_item<8>(a, it, g, sbase + kOffV, kVStageBytes, kVStages, bars.v_full, bars.v_empty, abort_flag,
-                             &range_err))
+        if constexpr (dense) {
+          if (warp == 1 && !produce_item_dense<8>(a, &kvmap, it, g, sbase + kOffV, kVStageBytes, kVStages, bars.v_full,
+                                                  bars.v_empty, abort_flag, &issued))
+            break;
+        } else if (!produce_item<8>(a, it, g, sbase + kOffV, kVStageBytes, kVStages, bars.v_full, bars.v_empty,
+                                    abort_flag, &range_err)) {
           break;
+        }
         g += it.n_tiles;
       }
+      if (dense && warp == 1 && *abort_flag) drain_dense(bars.v_full, kVStages, issued, a.limit_ns);
       ptx::cp_async_wait<0>();
       if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
     } else if (warp < kCreditWarp) {
@@ -809,14 +863,21 @@ cudaError_t launch_sparse_attn(const AttnArgs& a0, cudaStream_t stream) {
   const uint64_t rows = static_cast<uint64_t>(a.T) * a.H;
   if (!encode_tmap_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kDL, rows, kDL * 2, 64, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  // the latent rows as [n_kv_rows, 576] bf16, box 64 x 64: the dense causal mode's tile loads
+  CUtensorMap kvmap;
+  if (!encode_tmap_2d(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kDL, static_cast<uint64_t>(a.n_kv_rows), kDL * 2,
+                      64, kKT))
+    return cudaErrorInvalidValue;
+  const bool dense = a.idx == nullptr;
+  auto kernel = dense ? sparse_attn_kernel<true> : sparse_attn_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   // one cluster per SM pair, each taking every n_clusters-th work item
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t items = static_cast<int64_t>(a.T) * a.n_split;
   const int clusters = static_cast<int>(items < sms / 2 ? items : sms / 2);
-  sparse_attn_kernel<<<dim3(2 * clusters), kThreads, kSmem, stream>>>(a, qmap);
+  kernel<<<dim3(2 * clusters), kThreads, kSmem, stream>>>(a, qmap, kvmap);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_split == 1) return e;
   return launch_attn_combine(a, stream);

@@ -105,6 +105,14 @@ def test_topk_and_attention_reject_bad_arguments_on_host():
     assert s(A, A + 2, 10, None, 0, 0, A, 2, 8, 4, 0.1, A, None, None) == 1
     assert s(A, A, 0, None, 0, 0, A, 2, 8, 4, 0.1, A, None, None) == 1
     assert s(A, A, 10, None, 0, 0, A, 0, 8, 4, 0.1, A, None, None) == 0
+    d = dsa.lib.dsa_dense_causal_attn
+    assert d(A, A, 10, 2, 129, 0, 0.1, A, None, None) == 2          # H > 128
+    assert d(A, A, 10, 4, 8, 7, 0.1, A, None, None) == 1            # q_pos0 + T > n_kv_rows
+    assert d(A, A, 10, 2, 8, -1, 0.1, A, None, None) == 1           # negative position
+    assert d(A, A + 2, 10, 2, 8, 0, 0.1, A, None, None) == 1        # misaligned kv
+    assert d(None, A, 10, 2, 8, 0, 0.1, A, None, None) == 1
+    assert d(A, A, 1 << 31, 2, 8, 0, 0.1, A, None, None) == 1       # rows past int32
+    assert d(A, A, 10, 0, 8, 3, 0.1, A, None, None) == 0            # nothing to do
 
 
 def test_forward_workspace_and_validation():

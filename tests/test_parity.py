@@ -289,6 +289,46 @@ def test_attention_ragged_selection_and_range_errors(dsa):
     _check_attention(out2.float().cpu().numpy()[0], None, o_ref, None, "range row")
 
 
+@pytest.mark.parametrize("S,q_pos0,T,H", [(256, 0, 256, 8), (1000, 700, 300, 128), (130, 0, 130, 5)])
+def test_dense_causal_attention_matches_oracle(dsa, S, q_pos0, T, H):
+    # every row of the chunk at positions q_pos0 .. q_pos0 + T - 1, ragged last tiles included
+    g = torch.Generator().manual_seed(S + q_pos0 + H)
+    q = torch.randn(T, H, 576, generator=g).to(torch.bfloat16)
+    kv = torch.randn(S, 576, generator=g).to(torch.bfloat16)
+    out, lse = dsa.dense_causal_attn(q.cuda(), kv.cuda(), 0.07, q_pos0=q_pos0)
+    assert dsa.device_status() == 0
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    rows = range(T) if T * H <= 4096 else sorted({0, 1, 63, 64, 65, T // 2, T - 2, T - 1})
+    for t in rows:
+        o_ref, l_ref = oracle.dense_causal_row(q[t], kv, q_pos0 + t, 0.07)
+        _check_attention(out[t], lse[t], o_ref, l_ref, f"dense row {t}")
+
+
+def test_dense_causal_attention_4k_sampled_rows_and_sparse_equivalence(dsa):
+    # the 4K prefill shapes: dense rows against the oracle, and against the sparse kernel given the
+    # whole causal prefix as its selection (same arithmetic, same key order)
+    cfg = synth.config(2)
+    g = torch.Generator().manual_seed(5)
+    L, H = cfg.L, cfg.H
+    q = torch.randn(L, H, 576, generator=g).to(torch.bfloat16)
+    kv = torch.randn(L, 576, generator=g).to(torch.bfloat16)
+    qd, kvd = q.cuda(), kv.cuda()
+    out, lse = dsa.dense_causal_attn(qd, kvd, cfg.scale)
+    assert dsa.device_status() == 0
+    rows = [0, 63, 64, 1000, 2047, 2048, 4095]
+    o_np, l_np = out.float().cpu().numpy(), lse.cpu().numpy()
+    for t in rows:
+        o_ref, l_ref = oracle.dense_causal_row(q[t], kv, t, cfg.scale)
+        _check_attention(o_np[t], l_np[t], o_ref, l_ref, f"dense 4K row {t}")
+    sub = torch.tensor(rows)
+    idx = torch.arange(L, dtype=torch.int32).expand(len(rows), L).clone()
+    idx[idx > sub[:, None]] = -1
+    o_sp, l_sp = dsa.sparse_attn(qd[sub.cuda()].contiguous(), kvd, idx.cuda(), cfg.scale)
+    assert dsa.device_status() == 0
+    assert torch.equal(o_sp.cpu(), out[sub.cuda()].cpu())
+    assert torch.equal(l_sp.cpu(), lse[sub.cuda()].cpu())
+
+
 @pytest.mark.parametrize("n_split", [2, 3, 8])
 def test_attention_key_split_matches_oracle(dsa, n_split):
     g = torch.Generator().manual_seed(21 + n_split)
