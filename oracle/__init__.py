@@ -19,6 +19,9 @@ address; sections are the pages' own numbering):
       (same page, §2.1.2 output equation), MQA mode of MLA: one latent row
       c_s per token shared by every query head (same page, §2.2).  The value
       is the first 512 dims of the 576-dim latent, softmax scale 1/sqrt(192).
+  * indexer training loss: target p = head-summed attention probabilities over
+      the set, L1-normalised, and KL(p || Softmax(I)) (same page, §2.3.1 over all
+      s <= t in the dense warm-up, §2.3.2 over the selected set S_t).
   * dense causal attention over every row s <= t: the computation DSA replaces,
       which vpshk.cn/20260227158.html and 10100.com/article/43188788 §1 compare
       DSA's cost against.
@@ -33,6 +36,6 @@ brute-force enumeration and closed forms.
 """
 from .dsa import (  # noqa: F401
     e4m3_to_f64, bf16_bits_to_f64, indexer_row, indexer_scores, topk_row, topk_rows,
-    attention_row, dense_causal_row, prefill_row, prefill_rows, decode_row, decode_gather,
+    attention_row, dense_causal_row, indexer_kl_row, indexer_loss_prefill_row, prefill_row, prefill_rows, decode_row, decode_gather,
     selected_pairs, causal_pairs, index_sets_match, attention_error,
 )

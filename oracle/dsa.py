@@ -158,6 +158,59 @@ def dense_causal_row(q_t, kv, pos: int, scale: float, d_value: int = 512):
 
 
 # ----------------------------------------------------------------------------
+# Indexer training loss  ([digest] §2.3.1 dense warm-up, §2.3.2 sparse training)
+# ----------------------------------------------------------------------------
+
+
+def indexer_kl_row(q_t, latent_rows, scores_sel, scale: float):
+    """Target distribution and KL term of one query token over a key set.
+
+    [digest] §2.3.1: the main attention scores of all heads are summed and L1-normalised along the
+    keys into the target p; the indexer is fitted by KL(p || Softmax(I)).  §2.3.2 applies the same
+    loss over the selected set S_t only.  Reading: the "attention scores" are the per-head softmax
+    probabilities over the set (so p is their head average).  latent_rows [n, 576] are the rows of
+    the set, scores_sel [n] the indexer scores I[t, s] at the same keys.  Returns (p [n], kl);
+    an empty set gives (empty, 0.0).  0 * ln 0 is taken as 0.
+    """
+    q = bf16_bits_to_f64(_as_np(q_t))
+    c = bf16_bits_to_f64(_as_np(latent_rows))
+    n = c.shape[0]
+    if n == 0:
+        return np.zeros(0), 0.0
+    logits = scale * (q @ c.T)                                  # [H, n]
+    e = np.exp(logits - logits.max(axis=1, keepdims=True))
+    probs = e / e.sum(axis=1, keepdims=True)                    # softmax of each head over the set
+    u = probs.sum(axis=0)                                       # summed over heads
+    p = u / np.abs(u).sum()                                     # L1 normalisation along the keys
+    I = np.asarray(scores_sel, dtype=np.float64)
+    log_q = I - (I.max() + np.log(np.exp(I - I.max()).sum()))  # log Softmax(I) over the set
+    nz = p > 0
+    kl = float(np.sum(p[nz] * (np.log(p[nz]) - log_q[nz])))
+    return p, kl
+
+
+def indexer_loss_prefill_row(inp: dict, t: int, k: int, scale: float, q_pos0: int = 0, dense: bool = False,
+                             idx_override=None):
+    """Indexer-loss term of one prefill row at position q_pos0 + t.
+
+    dense=False: the sparse training stage, over the row's top-k set S_t (the oracle's own selection,
+    or idx_override).  dense=True: the dense warm-up stage, over every key s <= q_pos0 + t.
+    Returns dict(p, kl, keys) with the target p over `keys` (positions, in set order).
+    """
+    S = inp["k8"].shape[0]
+    n = min(S, q_pos0 + t + 1)
+    sc = indexer_row(inp["q8"][t], inp["q_scale"][t], inp["w"][t], inp["k8"], inp["k_scale"], n)
+    if dense:
+        keys = np.arange(n)
+    else:
+        keys = topk_row(sc, k) if idx_override is None else np.asarray(idx_override)
+        keys = keys[keys >= 0]
+    kv = _as_np(inp["kv"])
+    p, kl = indexer_kl_row(inp["q"][t], kv[keys], sc[keys], scale)
+    return dict(p=p, kl=kl, keys=keys)
+
+
+# ----------------------------------------------------------------------------
 # Whole forward, one query row at a time
 # ----------------------------------------------------------------------------
 

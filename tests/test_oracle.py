@@ -240,6 +240,62 @@ def test_attention_is_order_invariant_and_lse_matches_logsumexp():
     np.testing.assert_allclose(l1, ref_lse, rtol=1e-13)
 
 
+# ---------------------------------------------------------------- indexer loss
+
+def test_indexer_kl_matches_torch_softmax_and_scipy_rel_entr():
+    from scipy.special import rel_entr, softmax
+    g = torch.Generator().manual_seed(31)
+    H, n, scale = 5, 40, 0.09
+    q = torch.randn(H, 576, generator=g).to(torch.bfloat16)
+    c = torch.randn(n, 576, generator=g).to(torch.bfloat16)
+    I = torch.randn(n, generator=g, dtype=torch.float64) * 3
+    p, kl = oracle.indexer_kl_row(q, c, I.numpy(), scale)
+    # head average of each head's attention weights (each head's weights sum to one)
+    p_ref = torch.softmax(scale * (q.double() @ c.double().T), dim=1).mean(dim=0).numpy()
+    np.testing.assert_allclose(p, p_ref, rtol=1e-12, atol=1e-15)
+    assert abs(p.sum() - 1.0) < 1e-12
+    kl_ref = rel_entr(p_ref, softmax(I.numpy())).sum()
+    assert abs(kl - kl_ref) <= 1e-12 * max(1.0, abs(kl_ref))
+
+
+def test_indexer_kl_vanishes_when_the_indexer_reproduces_the_target():
+    g = torch.Generator().manual_seed(32)
+    q = torch.randn(3, 576, generator=g).to(torch.bfloat16)
+    c = torch.randn(25, 576, generator=g).to(torch.bfloat16)
+    p, _ = oracle.indexer_kl_row(q, c, np.zeros(25), 0.05)
+    _, kl = oracle.indexer_kl_row(q, c, np.log(p) + 3.7, 0.05)   # softmax(ln p + const) = p
+    assert abs(kl) < 1e-12
+
+
+def test_indexer_kl_binary_closed_form():
+    # one head, two keys: p = (sigmoid(a - b), ...), q = (sigmoid(x - y), ...)
+    q = torch.zeros(1, 576)
+    q[0, 0] = 2.0
+    c = torch.zeros(2, 576)
+    c[0, 0], c[1, 0] = 1.0, -0.5
+    a, b = 0.25 * 2.0 * 1.0, 0.25 * 2.0 * -0.5
+    x, y = 1.3, -0.4
+    p1, q1 = 1 / (1 + math.exp(-(a - b))), 1 / (1 + math.exp(-(x - y)))
+    want = p1 * math.log(p1 / q1) + (1 - p1) * math.log((1 - p1) / (1 - q1))
+    p, kl = oracle.indexer_kl_row(q.to(torch.bfloat16), c.to(torch.bfloat16), [x, y], 0.25)
+    np.testing.assert_allclose(p, [p1, 1 - p1], rtol=1e-14)
+    assert abs(kl - want) < 1e-14
+
+
+def test_indexer_loss_rows_dense_variant_and_nonnegativity():
+    cfg = synth.config(1, k=16)
+    inp = synth.prefill_inputs(cfg)
+    for t in [0, 5, 15, 16, 100, 255]:
+        d = oracle.indexer_loss_prefill_row(inp, t, cfg.k, cfg.scale, dense=True)
+        assert d["keys"].tolist() == list(range(t + 1))
+        full = oracle.indexer_loss_prefill_row(inp, t, cfg.k, cfg.scale, idx_override=np.arange(t + 1))
+        np.testing.assert_array_equal(d["p"], full["p"])
+        assert d["kl"] == full["kl"] and d["kl"] >= 0
+        sp = oracle.indexer_loss_prefill_row(inp, t, cfg.k, cfg.scale)
+        assert len(sp["keys"]) == min(t + 1, cfg.k) and sp["kl"] >= -1e-15
+        assert abs(sp["p"].sum() - 1) < 1e-12
+
+
 # ---------------------------------------------------------------- paging / decode
 
 def test_decode_paged_equals_contiguous_prefill_row():
