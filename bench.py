@@ -223,6 +223,8 @@ def run_ours(args, dist, rank, ws):
         return bench_prefill_tail(dsa, synth, args, peaks)
     if args.workload == "dense_curve":
         return bench_dense_curve(dsa, synth, args, peaks)
+    if args.workload == "indexer_loss":
+        return bench_indexer_loss(dsa, synth, args, peaks)
     cid = {"prefill128k": 4, "prefill4k": 2}[args.workload]
     cfg = synth.config(cid)
     if rank:
@@ -346,6 +348,27 @@ def bench_prefill_tail(dsa, synth, args, peaks, n_rows=1024):
         raise RuntimeError(f"device status {st}")
     kms = {k: round(_pairs_ms(v) / args.steps, 4) for k, v in ev.items()}
     ms = sum(kms.values())
+    # the other kernels on the same rows (run after the step, timed apart): the indexer loss over the
+    # selected sets, dense causal attention over every preceding key, and the dense warm-up loss
+    dense_lse = torch.empty_like(lse)
+    extras = {
+        "loss": lambda: dsa.indexer_loss(d["q"], d["kv"], lse, scores, cfg.scale, idx=idx, want_p=False),
+        "dense_attn": lambda: dsa.dense_causal_attn(d["q"], d["kv"], cfg.scale, q_pos0=r0, out=out, lse=dense_lse),
+        "dense_loss": lambda: dsa.indexer_loss(d["q"], d["kv"], dense_lse, scores, cfg.scale, q_pos0=r0),
+    }
+    for name, fn in extras.items():
+        for _ in range(max(3, args.warmup)):
+            fn()
+        e = []
+        for _ in range(args.steps):
+            e.append(_rec())
+            fn()
+            e.append(_rec())
+        torch.cuda.synchronize()
+        kms[name] = round(_pairs_ms(e) / args.steps, 4)
+    st = dsa.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
     return {"metric": "prefill tail tokens/s", "value": round(n_rows / (ms * 1e-3), 1), "unit": "tokens/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "dtype": "fp8-e4m3 / bf16", "data": "synthetic",
@@ -400,6 +423,85 @@ def bench_dense_curve(dsa, synth, args, peaks, lengths=(4096, 16384, 32768, 6553
             "config": {"workload": "one prefill sequence per L (128K recipe), H=128, k=2048, H_I=64",
                        "dense": "dsa_dense_causal_attn over the same Q and latent rows (no indexer, no top-k)"},
             "curve": curve}
+
+
+def bench_indexer_loss(dsa, synth, args, peaks, dense_L=32768):
+    """Training-side forward of the 128K prefill: per 8192-row chunk the indexer, top-k, sparse
+    attention (for lse) and the indexer's KL loss over the selected sets; plus the dense warm-up
+    stage (indexer, dense causal attention, KL over every preceding key) on a 32K sequence."""
+    out = {}
+    for stage, L in (("sparse", 131072), ("dense_warmup", dense_L)):
+        cfg = synth.config(4, L=L)
+        d = synth.prefill_inputs(cfg, device="cuda")
+        chunk = min(args.chunk, L)
+        ld = (L + 3) // 4 * 4
+        scores = torch.empty((chunk, ld), dtype=torch.float32, device="cuda")
+        idx = torch.empty((L, cfg.k), dtype=torch.int32, device="cuda")
+        o = torch.empty((L, cfg.H, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((L, cfg.H), dtype=torch.float32, device="cuda")
+        kl = torch.empty((L,), dtype=torch.float32, device="cuda")
+        p = torch.empty((chunk, cfg.k), dtype=torch.float32, device="cuda")
+        loss = torch.zeros((1,), dtype=torch.float64, device="cuda")
+        n_chunks = (L + chunk - 1) // chunk
+
+        def step(ev=None):
+            loss.zero_()
+            for c in range(n_chunks):
+                r0, r1 = c * chunk, min(L, (c + 1) * chunk)
+                sc = scores[: r1 - r0]
+                dsa.index(d["q8"][r0:r1], d["q_scale"][r0:r1], d["w"][r0:r1], d["k8"], d["k_scale"], q_pos0=r0,
+                          scores=sc)
+                if stage == "sparse":
+                    dsa.topk(sc, cfg.k, q_pos0=r0, n_cols=L, idx=idx[r0:r1])
+                    dsa.sparse_attn(d["q"][r0:r1], d["kv"], idx[r0:r1], cfg.scale, out=o[r0:r1], lse=lse[r0:r1])
+                else:
+                    dsa.dense_causal_attn(d["q"][r0:r1], d["kv"], cfg.scale, q_pos0=r0, out=o[r0:r1], lse=lse[r0:r1])
+                if ev is not None:
+                    ev.append(_rec())
+                if stage == "sparse":
+                    dsa.indexer_loss(d["q"][r0:r1], d["kv"], lse[r0:r1], sc, cfg.scale, idx=idx[r0:r1],
+                                     p=p[: r1 - r0], kl=kl[r0:r1], loss=loss)
+                else:
+                    dsa.indexer_loss(d["q"][r0:r1], d["kv"], lse[r0:r1], sc, cfg.scale, q_pos0=r0, kl=kl[r0:r1],
+                                     loss=loss)
+                if ev is not None:
+                    ev.append(_rec())
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        n = max(2, min(args.steps, 3))
+        ev = []
+        a = _rec()
+        for _ in range(n):
+            step(ev)
+        b = _rec()
+        b.synchronize()
+        st = dsa.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} ({stage})")
+        ms = a.elapsed_time(b) / n
+        loss_ms = _pairs_ms(ev) / n
+        pairs = (sum(min(t + 1, cfg.k) for t in range(min(L, cfg.k))) + max(0, L - cfg.k) * cfg.k
+                 if stage == "sparse" else L * (L + 1) // 2)
+        flop = 2.0 * cfg.H * 576 * pairs
+        tf = flop / (loss_ms * 1e-3) / 1e12
+        out[stage] = {"L": L, "step_ms": round(ms, 3), "tokens_per_s": round(L / (ms * 1e-3), 1),
+                      "loss_kernel_ms": round(loss_ms, 3), "loss_launches": n_chunks,
+                      "loss_kernel": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_sus"],
+                                      "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_sus"], 4),
+                                      "work": "2 H 576 FLOP per (row, key) pair of the set (QK^T recomputed)"},
+                      "loss_value": float(loss.item())}
+        del d, scores, idx, o, lse, kl, p
+        torch.cuda.empty_cache()
+    sp = out["sparse"]
+    return {"metric": "training-side prefill tokens/s with the indexer KL loss (128K, sparse stage)",
+            "value": sp["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1, "steps": max(2, min(args.steps, 3)),
+            "warmup": args.warmup, "ms_per_step": sp["step_ms"], "higher_is_better": True,
+            "dtype": "fp8-e4m3 indexer / bf16 attention and loss (fp32 accum, fp64 row sums)", "data": "synthetic",
+            "config": {"workload": "prefill L=131072 in 8192-row chunks: indexer, top-k, sparse attention, KL loss; "
+                                   f"dense warm-up stage at L={dense_L}"},
+            "stages": out}
 
 
 def bench_decode(dsa, synth, args, peaks, cid=5):
@@ -592,7 +694,7 @@ def main():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--chunk", type=int, default=8192)
     p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k", "prefill128k_tail", "decode", "decode32k",
-                                                       "dense_curve"],
+                                                       "dense_curve", "indexer_loss"],
                    help="the others run single pieces (used for profiler captures)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--e2e-chunk", type=int, default=2048, help="query rows per chunk of the host-buffer pipeline")

@@ -22,6 +22,10 @@
  *     a failed launch returns DSA_ERR_CUDA.  Device-side faults the kernels detect
  *     themselves (a wait that timed out, an index out of range) are recorded in a
  *     per-device status word that dsa_device_status() returns and clears.
+ *   - Every wait inside a kernel is bounded: after about one second it gives up, the
+ *     kernel records DSA_ERR_DEVICE_TIMEOUT and returns.  The environment variable
+ *     DSA_WAIT_LIMIT_MS (a positive integer, read once per process) sets another limit,
+ *     for profilers that slow kernels down by orders of magnitude.
  *   - No C++ exception crosses this boundary.  The functions are thread-safe as long
  *     as calls that share output buffers are ordered by the caller.
  *   - Pointers to FP8 / bf16 row data must be 16-byte aligned (the kernels move rows
@@ -38,6 +42,9 @@ extern "C" {
 #endif
 
 typedef struct CUstream_st* dsa_stream_t; /* identical to cudaStream_t */
+
+/* The bound, in nanoseconds, that every wait inside the kernels is given (host-only query). */
+uint64_t dsa_wait_limit_ns(void);
 
 typedef enum {
   DSA_OK = 0,
@@ -184,6 +191,34 @@ dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_
 dsa_status_t dsa_dense_causal_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, int T, int H,
                                    int64_t q_pos0, float scale, uint16_t* out, float* lse,
                                    dsa_stream_t stream);
+
+/*
+ * dsa_indexer_loss — the lightning indexer's training objective
+ * (freezhihu.org/question/1978819912970555965 §2.3.1 dense warm-up, §2.3.2 sparse training):
+ *     L^I = sum_t KL(p_t || Softmax(I[t, S_t]))
+ * where the target p_t is the main attention of all heads summed and L1-normalised over the
+ * keys of S_t (read here as the per-head softmax probabilities, so p_t is their head average).
+ *
+ *   idx non-NULL: sparse stage, S_t = the valid slots of idx [T, k] (as in dsa_sparse_attn).
+ *   idx NULL:     dense warm-up, S_t = every position 0 .. q_pos0 + t (q_pos0 >= 0,
+ *                 q_pos0 + T <= n_kv_rows and <= ld; p must be NULL; k and the slot layout unused).
+ *
+ *   q, kv, T, H, scale: as in dsa_sparse_attn (contiguous kv [n_kv_rows, 576], n_kv_rows < 2^31)
+ *   lse    [T, H] fp32: the natural-log softmax normalisers of the forward over the same sets
+ *          (the lse output of dsa_sparse_attn / dsa_dense_causal_attn); the head probabilities
+ *          are recomputed from q and kv as exp(scale * q . c_s - lse)
+ *   scores [T, ld] fp32 indexer scores I[t, s] at column s (dsa_index output); every position in
+ *          a set must be < ld (a larger one is skipped and reported as DSA_ERR_DEVICE_RANGE)
+ *   p      [T, k] fp32 target per slot (0 for empty slots), or NULL
+ *   kl     [T] fp32 KL term per row (0 for a row with an empty set), or NULL
+ *   loss_acc  one double: sum_t KL_t is ADDED to it (the caller zeroes it), or NULL
+ * The scores QK^T are recomputed on the tensor cores (bf16 inputs, fp32 accumulation); the
+ * head sums in fp32; the per-row sums in fp64.  Errors as in dsa_sparse_attn.
+ */
+dsa_status_t dsa_indexer_loss(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* idx,
+                              int T, int H, int k, int64_t q_pos0, float scale, const float* lse,
+                              const float* scores, int64_t ld, float* p, float* kl, double* loss_acc,
+                              dsa_stream_t stream);
 
 /* Forward modes. */
 enum { DSA_MODE_PREFILL = 0, DSA_MODE_DECODE = 1 };

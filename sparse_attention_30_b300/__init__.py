@@ -25,7 +25,7 @@ EXPORTS = ("dsa_status_string", "dsa_version", "dsa_index", "dsa_index_paged", "
            "dsa_forward_workspace_size", "dsa_forward", "dsa_device_status", "dsa_selftest_wait_timeout",
            "dsa_decode_noalloc", "dsa_decode_noalloc_capacity", "dsa_sparse_attn_split_workspace_size",
            "dsa_sparse_attn_split", "dsa_prefill_host_workspace_size", "dsa_prefill_host",
-           "dsa_dense_causal_attn")
+           "dsa_dense_causal_attn", "dsa_indexer_loss", "dsa_wait_limit_ns")
 
 
 class DSAError(RuntimeError):
@@ -74,6 +74,8 @@ def _load():
         "dsa_decode_noalloc_capacity": ([], ctypes.c_size_t),
         "dsa_sparse_attn_split_workspace_size": ([I, I, I], ctypes.c_size_t),
         "dsa_dense_causal_attn": ([P, P, I64, I, I, I64, F, P, P, P], I),
+        "dsa_wait_limit_ns": ([], ctypes.c_uint64),
+        "dsa_indexer_loss": ([P, P, I64, P, I, I, I, I64, F, P, P, I64, P, P, P, P], I),
         "dsa_sparse_attn_split": ([P, P, I64, P, I64, I, P, I, I, I, F, P, P, I, P, ctypes.c_size_t, P], I),
         "dsa_prefill_host_workspace_size": ([ctypes.POINTER(ForwardArgs)], ctypes.c_size_t),
         "dsa_prefill_host": ([ctypes.POINTER(ForwardArgs), P, ctypes.c_size_t, P], I),
@@ -197,6 +199,33 @@ def dense_causal_attn(q, kv, scale, q_pos0=0, out=None, lse=None, want_lse=True)
     _check(lib.dsa_dense_causal_attn(_ptr(q), _ptr(kv), kv.shape[0], T, H, int(q_pos0), float(scale), _ptr(out),
                                      _ptr(lse), _stream(q)), "dsa_dense_causal_attn")
     return out, lse
+
+
+def indexer_loss(q, kv, lse, scores, scale, idx=None, q_pos0=0, p=None, kl=None, loss=None, want_p=True):
+    """The indexer's KL training loss (dsa_indexer_loss).  idx [T, k] selects the sparse stage (target
+    over each row's selected set); idx=None is the dense warm-up over every position <= q_pos0 + t.
+    lse [T, H] comes from the forward over the same sets, scores [T, ld] from the indexer.
+    Returns (p [T, k] | None, kl [T], loss) with loss a float64 tensor of one element (summed over rows,
+    added to `loss` when one is passed)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv, torch.bfloat16, "kv", 2)
+    _need(lse, torch.float32, "lse", 2)
+    _need(scores, torch.float32, "scores", 2)
+    T, H, _ = q.shape
+    k = 0
+    if idx is not None:
+        _need(idx, torch.int32, "idx", 2)
+        k = idx.shape[1]
+        if p is None and want_p:
+            p = torch.empty((T, k), dtype=torch.float32, device=q.device)
+    if kl is None:
+        kl = torch.empty((T,), dtype=torch.float32, device=q.device)
+    if loss is None:
+        loss = torch.zeros((1,), dtype=torch.float64, device=q.device)
+    _check(lib.dsa_indexer_loss(_ptr(q), _ptr(kv), kv.shape[0], _ptr(idx), T, H, k, int(q_pos0), float(scale),
+                                _ptr(lse), _ptr(scores), scores.stride(0), _ptr(p), _ptr(kl), _ptr(loss), _stream(q)),
+           "dsa_indexer_loss")
+    return p, kl, loss
 
 
 def decode_split(B: int) -> int:

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "dsa_internal.h"
@@ -79,6 +80,18 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                        uint32_t box_rows) {
   return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, rows, inner, box_inner, box_rows);
+}
+
+uint64_t wait_limit_ns() {
+  static const uint64_t limit = []() -> uint64_t {
+    const char* e = std::getenv("DSA_WAIT_LIMIT_MS");
+    if (e == nullptr) return kWaitLimitNs;
+    char* end = nullptr;
+    const long long ms = std::strtoll(e, &end, 10);
+    if (end == e || *end != '\0' || ms <= 0 || ms > 3600000) return kWaitLimitNs;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return limit;
 }
 
 cudaError_t launch_wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {
@@ -243,6 +256,8 @@ bool copy_streams(cudaStream_t* in, cudaStream_t* out) {
 
 extern "C" {
 
+uint64_t dsa_wait_limit_ns(void) { return wait_limit_ns(); }
+
 const char* dsa_status_string(dsa_status_t s) {
   switch (s) {
     case DSA_OK: return "DSA_OK";
@@ -268,7 +283,7 @@ dsa_status_t dsa_index(const uint8_t* q8, const float* q_scale, const float* w, 
   IndexerArgs a{};
   a.q_scale = q_scale; a.w = w; a.k_scale = k_scale;
   a.scores = scores; a.ld = ld; a.rows = T; a.S = S; a.q_pos0 = q_pos0;
-  a.status = status; a.limit_ns = kWaitLimitNs;
+  a.status = status; a.limit_ns = wait_limit_ns();
   const int max_keys = static_cast<int>(std::min<int64_t>(S, q_pos0 + T));
   return from_cuda(launch_indexer(q8, k8, S, H_I, false, max_keys, a, stream));
 }
@@ -286,7 +301,7 @@ dsa_status_t dsa_index_paged(const uint8_t* q8, const float* q_scale, const floa
   a.q_scale = q_scale; a.w = w; a.k_scale = k_scale_cache;
   a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens; a.n_pages = n_pages;
   a.scores = scores; a.ld = ld; a.rows = B; a.S = max_seq_len; a.page_size = page_size;
-  a.status = status; a.limit_ns = kWaitLimitNs;
+  a.status = status; a.limit_ns = wait_limit_ns();
   return from_cuda(launch_indexer(q8, k8_cache, n_pages * page_size, H_I, true, max_seq_len, a, stream));
 }
 
@@ -311,7 +326,7 @@ dsa_status_t sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_t n_
   a.q = q; a.kv = kv; a.n_kv_rows = n_kv_rows; a.block_table = block_table; a.bt_stride = bt_stride;
   a.page_size = page_size; a.idx = idx; a.T = T; a.H = H; a.k = k;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.out = out; a.lse = lse; a.status = status; a.limit_ns = kWaitLimitNs;
+  a.out = out; a.lse = lse; a.status = status; a.limit_ns = wait_limit_ns();
   a.n_split = n_split; a.part_o = part_o; a.part_ml = part_ml;
   return from_cuda(launch_sparse_attn(a, stream));
 }
@@ -370,7 +385,33 @@ extern "C" dsa_status_t dsa_dense_causal_attn(const uint16_t* q, const uint16_t*
   AttnArgs a{};
   a.q = q; a.kv = kv; a.n_kv_rows = n_kv_rows; a.idx = nullptr; a.T = T; a.H = H; a.k = 0; a.q_pos0 = q_pos0;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.out = out; a.lse = lse; a.status = status; a.limit_ns = kWaitLimitNs; a.n_split = 1;
+  a.out = out; a.lse = lse; a.status = status; a.limit_ns = wait_limit_ns(); a.n_split = 1;
+  return from_cuda(launch_sparse_attn(a, stream));
+}
+
+extern "C" dsa_status_t dsa_indexer_loss(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* idx,
+                                         int T, int H, int k, int64_t q_pos0, float scale, const float* lse,
+                                         const float* scores, int64_t ld, float* p, float* kl, double* loss_acc,
+                                         dsa_stream_t stream) {
+  if (T < 0 || H < 1 || n_kv_rows < 1 || n_kv_rows > INT32_MAX || ld < 1) return DSA_ERR_INVALID_ARG;
+  if (!q || !kv || !lse || !scores || !aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
+  if (idx) {
+    if (k < 1 || k > 65536) return DSA_ERR_INVALID_ARG;
+  } else {
+    // dense warm-up: every position up to the row's own, so the rows must fit the keys and scores
+    if (p || q_pos0 < 0 || q_pos0 + static_cast<int64_t>(T) > n_kv_rows || q_pos0 + static_cast<int64_t>(T) > ld)
+      return DSA_ERR_INVALID_ARG;
+  }
+  if (H > 128) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  int* status = status_ptr();
+  if (!status) return DSA_ERR_CUDA;
+  AttnArgs a{};
+  a.q = q; a.kv = kv; a.n_kv_rows = n_kv_rows; a.idx = idx; a.T = T; a.H = H; a.k = idx ? k : 0;
+  a.q_pos0 = idx ? 0 : q_pos0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status; a.limit_ns = wait_limit_ns(); a.n_split = 1;
+  a.lse_in = lse; a.scores = scores; a.ld = ld; a.p_out = p; a.kl_out = kl; a.loss_acc = loss_acc;
   return from_cuda(launch_sparse_attn(a, stream));
 }
 

@@ -11,6 +11,9 @@ namespace dsa {
 
 // Bounded waits give up after this long (about one second).
 constexpr uint64_t kWaitLimitNs = 1ull << 30;
+// The limit the kernels are given: kWaitLimitNs, or DSA_WAIT_LIMIT_MS milliseconds when that
+// environment variable holds a positive integer (read once; for tools that slow kernels down).
+uint64_t wait_limit_ns();
 
 // 2-D tensor map over a row-major matrix [rows, inner] with the given row pitch, 128-byte swizzle,
 // box [box_inner, box_rows]; false if the driver rejects it.
@@ -84,6 +87,14 @@ struct AttnArgs {
   int n_split;
   float* part_o;              // [T, n_split, H, 512] fp32, each normalised by its own sum
   float* part_ml;             // [T, n_split, H, 2] fp32: running max (log2 domain) and sum
+  // indexer-loss mode (lse_in non-NULL): no attention output; the head-summed attention target
+  // over each row's set and its KL divergence from the softmax of the indexer scores
+  const float* lse_in;        // [T, H] natural-log normalisers of the forward over the same sets
+  const float* scores;        // [T, ld] indexer scores, column = key position
+  int64_t ld;
+  float* p_out;               // [T, k] L1-normalised target per slot (0 for empty slots), or NULL
+  float* kl_out;              // [T] KL(p || softmax(I)) per row, or NULL
+  double* loss_acc;           // sum over rows added here, or NULL
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream);

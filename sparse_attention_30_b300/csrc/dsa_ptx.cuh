@@ -245,6 +245,10 @@ template <int SRC_BYTES>
 __device__ __forceinline__ void cp_async16_n(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "n"(SRC_BYTES) : "memory");
 }
+// 4-byte asynchronous copy global -> shared (through L1), tracked by commit / wait groups.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

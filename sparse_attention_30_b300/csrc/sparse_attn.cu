@@ -280,11 +280,199 @@ __device__ __forceinline__ void drain_dense(uint64_t* full, int stages, int issu
     drain_wait(baddr(full[gi % stages]), (gi / stages) & 1, limit_ns);
 }
 
-// kDense: dense causal mode (no selection; row t attends latent rows 0 .. q_pos0 + t).
+
+// Indexer-loss mode: the four row warps of a score CTA (one head row per thread).  For every key s
+// of token t's set, u_s = sum over heads of that head's attention probability
+// 2^(S[h,s] * scale * log2(e) - lse[h] * log2(e)), with the forward's own normalisers lse.  Each warp
+// sums its 32 heads with a butterfly that leaves keys 2*lane and 2*lane+1 on each lane, the four
+// warps meet in shared memory, and threads h < 64 then own key h of every tile: they decide whether
+// the key is in the set and accumulate, per token, U = sum u, A = sum u ln u, B = sum u I and the
+// log-sum-exp Z of I over the set.  At the token's end, with p = u / U and q = softmax(I):
+//     KL(p || q) = (A - B) / U - ln U + Z.
+// A key owner's position (from the selection) and indexer score arrive by asynchronous copies into
+// shared memory, the position two tiles and the score one tile ahead of use.
 template <bool kDense>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap,
-                       const __grid_constant__ CUtensorMap kvmap) {
+__device__ __forceinline__ void loss_row_warps(const AttnArgs& a, Bars& bars, const Item* sched, uint8_t* smem,
+                                               uint32_t tmem, volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = (warp & 3) * 32 + lane;
+  const bool owner = h < kKT;
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  float* red = reinterpret_cast<float*>(smem + kOffStage);             // [2 tiles][4 warps][64 keys]
+  double* fin = reinterpret_cast<double*>(smem + kOffStage + 2048);    // [2 warps][5] partials, then 1/U
+  double* acc = reinterpret_cast<double*>(smem + kOffStage + 4096) + h * 4;       // owner's U, A, B, sum e^(I-max)
+  float* acc_max = reinterpret_cast<float*>(smem + kOffStage + 6144) + h;        // owner's running max of I
+  int32_t* posb = reinterpret_cast<int32_t*>(smem + kOffStage + 6400);           // [2][64] selected positions
+  float* scb = reinterpret_cast<float*>(smem + kOffStage + 6912);                // [2][64] their scores
+  const uint32_t posb_s = ptx::smem_addr(posb + h), scb_s = ptx::smem_addr(scb + h);
+  int g = 0;
+  bool ok = true, range_err = false;
+  for (int j = 0; ok; ++j) {
+    Item it;
+    if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
+    const int t = it.t;
+    const int32_t* idx_row = kDense ? nullptr : a.idx + static_cast<int64_t>(t) * a.k;
+    const float* score_row = a.scores + static_cast<int64_t>(t) * a.ld;
+    const float lse2 = h < a.H ? a.lse_in[static_cast<int64_t>(t) * a.H + h] * 1.4426950408889634f : 0.f;
+    // key h of tile i: its slot, and (once its selection entry has landed) its position or -1
+    auto slot_of = [&](int i) { return (it.tile0 + i) * kKT + h; };
+    auto issue_idx = [&](int i) {  // selection entry of tile i -> posb[i & 1]
+      if (!kDense && i < it.n_tiles && slot_of(i) < a.k) ptx::cp_async4(posb_s + (i & 1) * kKT * 4, idx_row + slot_of(i));
+    };
+    auto position = [&](int i) -> int {
+      if (i >= it.n_tiles) return -1;
+      const int slot = slot_of(i);
+      if constexpr (kDense) {
+        return slot <= a.q_pos0 + t ? slot : -1;
+      } else {
+        const int32_t sidx = slot < a.k ? posb[(i & 1) * kKT + h] : -1;
+        return latent_row(a, t, sidx, &range_err) >= 0 ? sidx : -1;
+      }
+    };
+    auto issue_score = [&](int i, int pos) {  // score of tile i's key -> scb[i & 1]
+      if (pos >= 0 && pos < a.ld) ptx::cp_async4(scb_s + (i & 1) * kKT * 4, score_row + pos);
+    };
+    int pos = -1;
+    if (owner) {
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.0;
+      *acc_max = -INFINITY;
+      issue_idx(0);
+      issue_idx(1);
+      ptx::cp_async_commit();
+      ptx::cp_async_wait<0>();
+      pos = position(0);
+      issue_score(0, pos);
+      ptx::cp_async_commit();
+    }
+    for (int i = 0; i < it.n_tiles; ++i) {
+      const int gi = g + i, sb = gi % kSBufs;
+      const bool got = warp_wait(baddr(bars.s_full[sb]), (gi / kSBufs) & 1, abort_flag, a);
+      uint32_t s0[32], s1[32];
+      if (got) {
+        ptx::tc_fence_after();
+        ptx::tmem_ld32(tmem + kColS + sb * kKT + lane_base, s0);
+        ptx::tmem_ld32(tmem + kColS + sb * kKT + 32 + lane_base, s1);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(baddr(bars.s_empty[sb]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s0[e] = s1[e] = 0;
+      }
+      // every key of the tile (keys outside the set are dropped by their owners below)
+      float v[kKT];
+#pragma unroll
+      for (int e = 0; e < kKT; ++e) {
+        const uint32_t raw = e < 32 ? s0[e] : s1[e - 32];
+        v[e] = h < a.H ? fast_exp2(__uint_as_float(raw) * a.scale_log2 - lse2) : 0.f;
+      }
+      // sum over the warp's 32 heads; after the stage exchanging across lane bit sh, each lane keeps
+      // the half of its remaining keys selected by that bit
+#pragma unroll
+      for (int n = kKT; n > 2; n >>= 1) {
+        const int sh = n >> 2;  // n = 64, 32, 16, 8, 4 -> lane bit 16, 8, 4, 2, 1
+        const bool up = (lane & sh) != 0;
+#pragma unroll
+        for (int e = 0; e < n / 2; ++e) {
+          const float send = up ? v[e] : v[e + n / 2];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
+          v[e] = (up ? v[e + n / 2] : v[e]) + recv;
+        }
+      }
+      float* rb = red + (gi & 1) * (4 * kKT);
+      *reinterpret_cast<float2*>(rb + (warp & 3) * kKT + 2 * lane) = make_float2(v[0], v[1]);
+      if (ptx::named_sync_or(1, 128, !got || *abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (owner) {
+        ptx::cp_async_wait<0>();  // this tile's score and the next tile's selection entry
+        const int slot = slot_of(i);
+        if (pos >= 0 && pos < a.ld) {
+          const float u = rb[h] + rb[kKT + h] + rb[2 * kKT + h] + rb[3 * kKT + h];
+          const float I = scb[(i & 1) * kKT + h];
+          acc[0] += u;
+          if (u > 0.f) acc[1] += static_cast<double>(u) * logf(u);
+          acc[2] += static_cast<double>(u) * I;
+          const float zmax = *acc_max;
+          if (I > zmax) {
+            acc[3] = acc[3] * (zmax == -INFINITY ? 0.0 : static_cast<double>(expf(zmax - I))) + 1.0;
+            *acc_max = I;
+          } else {
+            acc[3] += expf(I - zmax);
+          }
+          if (!kDense && a.p_out) a.p_out[static_cast<int64_t>(t) * a.k + slot] = u;
+        } else {
+          if (pos >= a.ld) range_err = true;
+          if (!kDense && a.p_out && slot < a.k) a.p_out[static_cast<int64_t>(t) * a.k + slot] = 0.f;
+        }
+        pos = position(i + 1);
+        issue_score(i + 1, pos);
+        issue_idx(i + 2);
+        ptx::cp_async_commit();
+      }
+    }
+    if (owner) ptx::cp_async_wait<0>();  // nothing in flight into the buffers the next token reuses
+    // ---- the token's totals: owners h < 64 are warps (h / 32) = 0 and 1 of the four
+    if (owner) {
+      double U = acc[0], A = acc[1], B = acc[2], zsum = acc[3];
+      float zmax = *acc_max;
+#pragma unroll
+      for (int sh = 16; sh >= 1; sh >>= 1) {
+        U += __shfl_xor_sync(0xffffffffu, U, sh);
+        A += __shfl_xor_sync(0xffffffffu, A, sh);
+        B += __shfl_xor_sync(0xffffffffu, B, sh);
+        const float om = __shfl_xor_sync(0xffffffffu, zmax, sh);
+        const double os = __shfl_xor_sync(0xffffffffu, zsum, sh);
+        const float m = fmaxf(zmax, om);
+        zsum = (zmax == -INFINITY ? 0.0 : zsum * expf(zmax - m)) + (om == -INFINITY ? 0.0 : os * expf(om - m));
+        zmax = m;
+      }
+      if (lane == 0) {
+        double* f = fin + (h >> 5) * 5;
+        f[0] = U; f[1] = A; f[2] = B; f[3] = zmax; f[4] = zsum;
+      }
+    }
+    ptx::named_sync(2, 128);
+    if (h == 0) {
+      double Ut = 0.0, At = 0.0, Bt = 0.0, zs = 0.0;
+      float zm = -INFINITY;
+      for (int w = 0; w < 2; ++w) {
+        const double* f = fin + w * 5;
+        Ut += f[0]; At += f[1]; Bt += f[2];
+        const float m = fmaxf(zm, static_cast<float>(f[3]));
+        zs = (zm == -INFINITY ? 0.0 : zs * exp(static_cast<double>(zm - m))) +
+             (f[3] == -INFINITY ? 0.0 : f[4] * exp(f[3] - m));
+        zm = m;
+      }
+      const bool has = ok && it.n_tiles > 0 && Ut > 0.0;
+      const double kl = has ? (At - Bt) / Ut - log(Ut) + (zm + log(zs)) : 0.0;
+      if (ok) {
+        if (a.kl_out) a.kl_out[t] = static_cast<float>(kl);
+        if (a.loss_acc) atomicAdd(a.loss_acc, kl);
+      }
+      fin[10] = has ? 1.0 / Ut : 0.0;
+    }
+    ptx::named_sync(2, 128);
+    if (ok && !kDense && a.p_out && owner) {
+      // normalise the row's target (the entries this thread wrote) and clear the slots past its tiles
+      const float inv = static_cast<float>(fin[10]);
+      float* prow = a.p_out + static_cast<int64_t>(t) * a.k;
+      for (int slot = it.tile0 * kKT + h; slot < (it.tile0 + it.n_tiles) * kKT && slot < a.k; slot += kKT)
+        prow[slot] *= inv;
+      for (int slot = (it.tile0 + it.n_tiles) * kKT + h; slot < a.k; slot += kKT) prow[slot] = 0.f;
+    }
+    ptx::named_sync(2, 128);  // fin is reused by the next token
+    g += it.n_tiles;
+  }
+  if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
+}
+
+// kMode bit 0: dense causal (no selection; row t attends latent rows 0 .. q_pos0 + t).
+// kMode bit 1: indexer loss (no value pass; every CTA is an independent score CTA, launched without
+// clusters).  Attention modes run as clusters of two.
+template <int kMode>
+__device__ __forceinline__ void attn_body(const AttnArgs& a, const CUtensorMap* qmap, const CUtensorMap* kvmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -293,8 +481,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag_s;
 
-  const int rank = static_cast<int>(ptx::cluster_ctarank());
-  const int cl = blockIdx.x >> 1, n_cl = gridDim.x >> 1;
+  constexpr bool kDense = (kMode & 1) != 0, kLoss = (kMode & 2) != 0;
+  const int rank = kLoss ? 0 : static_cast<int>(ptx::cluster_ctarank());
+  const int cl = kLoss ? blockIdx.x : blockIdx.x >> 1, n_cl = kLoss ? gridDim.x : gridDim.x >> 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &abort_flag_s;
   const uint32_t sbase = ptx::smem_addr(smem);
@@ -353,7 +542,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == kSchedWarp) {
     // ================================================================ scheduler (both CTAs)
-    const int n_items = a.T * a.n_split;
+    const int n_items = a.T * a.n_split;  // (the loss modes run without a key split)
     for (int j = 0;; ++j) {
       const int slot = j % kSched;
       // the ring runs items ahead: this wait is never urgent, so it sleeps between polls
@@ -401,7 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_expect_tx(baddr(bars.q_full), kQBytes);
 #pragma unroll 1
           for (int b = 0; b < 9; ++b)
-            ptx::tma_load_2d_hint(sbase + kOffK + b * kQBoxBytes, &qmap, baddr(bars.q_full), b * 64, it.t * a.H,
+            ptx::tma_load_2d_hint(sbase + kOffK + b * kQBoxBytes, qmap, baddr(bars.q_full), b * 64, it.t * a.H,
                                   ptx::l2_evict_first_policy());  // Q and O stream: keep L2 for latent rows
         }
         __syncwarp();
@@ -466,7 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // every producer has read Q out of the ring before any of them overwrites it
         if (!got || !warp_wait(baddr(bars.q_ready), nq & 1, abort_flag, a)) break;
         if constexpr (dense) {
-          if (warp == 1 && !produce_item_dense<9>(a, &kvmap, it, g, sbase + kOffK, kKStageBytes, kKStages, bars.k_full,
+          if (warp == 1 && !produce_item_dense<9>(a, kvmap, it, g, sbase + kOffK, kKStageBytes, kKStages, bars.k_full,
                                                   bars.k_empty, abort_flag, &issued))
             break;
         } else if (!produce_item<9>(a, it, g, sbase + kOffK, kKStageBytes, kKStages, bars.k_full, bars.k_empty,
@@ -479,6 +668,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (dense && warp == 1 && *abort_flag) drain_dense(bars.k_full, kKStages, issued, a.limit_ns);
       ptx::cp_async_wait<0>();  // nothing of this thread's may still be in flight when the CTA exits
       if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
+    } else if (warp < kCreditWarp && kLoss) {
+      loss_row_warps<kDense>(a, bars, sched, smem, tmem, abort_flag);
     } else if (warp < kCreditWarp) {
       // ---- online softmax, one head row per thread
       const int h = (warp & 3) * 32 + lane;
@@ -665,7 +856,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!read_item(bars, sched, j, &it, abort_flag, a) || it.t < 0) break;
         if (it.n_tiles == 0) continue;
         if constexpr (dense) {
-          if (warp == 1 && !produce_item_dense<8>(a, &kvmap, it, g, sbase + kOffV, kVStageBytes, kVStages, bars.v_full,
+          if (warp == 1 && !produce_item_dense<8>(a, kvmap, it, g, sbase + kOffV, kVStageBytes, kVStages, bars.v_full,
                                                   bars.v_empty, abort_flag, &issued))
             break;
         } else if (!produce_item<8>(a, it, g, sbase + kOffV, kVStageBytes, kVStages, bars.v_full, bars.v_empty,
@@ -825,6 +1016,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap kvmap) {
+  attn_body<kMode>(a, &qmap, &kvmap);
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_loss_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                        const __grid_constant__ CUtensorMap kvmap) {
+  attn_body<kMode | 2>(a, &qmap, &kvmap);
+}
+
 // Merges the key-split partial results of one (token, head) row: with per-split running max m_s
 // (log2 domain), sum l_s and normalised output O_s, the row's softmax weights over the union of the
 // splits give O = sum_s l_s 2^(m_s - m) O_s / sum_s l_s 2^(m_s - m), m = max_s m_s.
@@ -854,31 +1059,58 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
 
 }  // namespace
 
+namespace {
+template <int kMode>
+cudaError_t launch_mode(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kvmap, int ctas,
+                        cudaStream_t stream) {
+  auto kernel = (kMode & 2) ? indexer_loss_kernel<kMode & 1> : sparse_attn_kernel<kMode & 1>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (kMode & 2) ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a, qmap, kvmap);
+}
+}  // namespace
+
 cudaError_t launch_sparse_attn(const AttnArgs& a0, cudaStream_t stream) {
   if (a0.T <= 0) return cudaSuccess;
   AttnArgs a = a0;
-  if (a.n_split < 1 || a.part_o == nullptr || a.part_ml == nullptr) a.n_split = 1;
+  const bool loss = a.lse_in != nullptr;
+  if (loss || a.n_split < 1 || a.part_o == nullptr || a.part_ml == nullptr) a.n_split = 1;
   // Q viewed as [T*H, 576] bf16, box 64 x 128 (rows past the tensor read as zero)
   CUtensorMap qmap;
   const uint64_t rows = static_cast<uint64_t>(a.T) * a.H;
   if (!encode_tmap_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kDL, rows, kDL * 2, 64, 128))
     return cudaErrorInvalidValue;
-  // the latent rows as [n_kv_rows, 576] bf16, box 64 x 64: the dense causal mode's tile loads
+  // the latent rows as [n_kv_rows, 576] bf16, box 64 x 64: the dense causal modes' tile loads
   CUtensorMap kvmap;
   if (!encode_tmap_2d(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kDL, static_cast<uint64_t>(a.n_kv_rows), kDL * 2,
                       64, kKT))
     return cudaErrorInvalidValue;
-  const bool dense = a.idx == nullptr;
-  auto kernel = dense ? sparse_attn_kernel<true> : sparse_attn_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e != cudaSuccess) return e;
-  // one cluster per SM pair, each taking every n_clusters-th work item
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t items = static_cast<int64_t>(a.T) * a.n_split;
+  const bool dense = a.idx == nullptr;
+  cudaError_t e;
+  if (loss) {
+    // one independent score CTA per SM, each taking every gridDim-th token
+    const int ctas = static_cast<int>(items < sms ? items : sms);
+    e = dense ? launch_mode<3>(a, qmap, kvmap, ctas, stream) : launch_mode<2>(a, qmap, kvmap, ctas, stream);
+    return e;
+  }
+  // one cluster per SM pair, each taking every n_clusters-th work item
   const int clusters = static_cast<int>(items < sms / 2 ? items : sms / 2);
-  kernel<<<dim3(2 * clusters), kThreads, kSmem, stream>>>(a, qmap, kvmap);
-  e = cudaGetLastError();
+  e = dense ? launch_mode<1>(a, qmap, kvmap, 2 * clusters, stream) : launch_mode<0>(a, qmap, kvmap, 2 * clusters, stream);
   if (e != cudaSuccess || a.n_split == 1) return e;
   return launch_attn_combine(a, stream);
 }

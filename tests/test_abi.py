@@ -113,6 +113,35 @@ def test_topk_and_attention_reject_bad_arguments_on_host():
     assert d(None, A, 10, 2, 8, 0, 0.1, A, None, None) == 1
     assert d(A, A, 1 << 31, 2, 8, 0, 0.1, A, None, None) == 1       # rows past int32
     assert d(A, A, 10, 0, 8, 3, 0.1, A, None, None) == 0            # nothing to do
+    L = dsa.lib.dsa_indexer_loss
+    #        q  kv  n   idx   T  H  k  pos0 scale lse scores ld  p     kl    loss  stream
+    assert L(A, A, 10, A, 2, 129, 4, 0, 0.1, A, A, 16, None, None, None, None) == 2     # H > 128
+    assert L(A, A, 10, A, 2, 8, 0, 0, 0.1, A, A, 16, None, None, None, None) == 1       # k = 0
+    assert L(A, A, 10, A, 2, 8, 4, 0, 0.1, None, A, 16, None, None, None, None) == 1    # no lse
+    assert L(A, A, 10, A, 2, 8, 4, 0, 0.1, A, None, 16, None, None, None, None) == 1    # no scores
+    assert L(A, A, 10, None, 4, 8, 0, 7, 0.1, A, A, 16, None, None, None, None) == 1    # dense: rows past keys
+    assert L(A, A, 20, None, 4, 8, 0, 7, 0.1, A, A, 10, None, None, None, None) == 1    # dense: rows past ld
+    assert L(A, A, 20, None, 4, 8, 0, 0, 0.1, A, A, 10, A, None, None, None) == 1       # dense: no per-slot target
+    assert L(A, A + 2, 10, A, 2, 8, 4, 0, 0.1, A, A, 16, None, None, None, None) == 1   # misaligned kv
+    assert L(A, A, 10, A, 0, 8, 4, 0, 0.1, A, A, 16, None, None, None, None) == 0       # nothing to do
+
+
+def test_wait_limit_default_and_environment_override():
+    import subprocess
+    import sys
+    code = "import sparse_attention_30_b300 as d; print(d.lib.dsa_wait_limit_ns())"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    def run(env_value):
+        env = dict(os.environ)
+        env.pop("DSA_WAIT_LIMIT_MS", None)
+        if env_value is not None:
+            env["DSA_WAIT_LIMIT_MS"] = env_value
+        out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, check=True)
+        return int(out.stdout.strip().splitlines()[-1])
+    assert run(None) == 1 << 30
+    assert run("30000") == 30000 * 1000000
+    for bad in ("0", "-5", "12ms", "", "99999999999"):
+        assert run(bad) == 1 << 30
 
 
 def test_forward_workspace_and_validation():

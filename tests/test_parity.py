@@ -329,6 +329,88 @@ def test_dense_causal_attention_4k_sampled_rows_and_sparse_equivalence(dsa):
     assert torch.equal(l_sp.cpu(), lse[sub.cuda()].cpu())
 
 
+KL_REL, P_REL = 1e-3, 1e-3
+
+
+def _check_loss(p_gpu, kl_gpu, ref, where):
+    """Target p within P_REL of the largest target entry (+1e-7), KL within KL_REL * max(1, |KL|)."""
+    if p_gpu is not None:
+        n = len(ref["p"])
+        assert np.all(p_gpu[n:] == 0), f"{where}: empty slots not zero"
+        err = np.abs(p_gpu[:n] - ref["p"]).max() if n else 0.0
+        assert err <= P_REL * (ref["p"].max() if n else 0) + 1e-7, f"{where}: p err {err:.3g}"
+    d = abs(float(kl_gpu) - ref["kl"])
+    assert d <= KL_REL * max(1.0, abs(ref["kl"])), f"{where}: kl {kl_gpu} vs {ref['kl']}"
+
+
+def _gpu_scores_idx_lse(dsa, d, cfg, q_pos0=0):
+    L = d["q8"].shape[0]
+    S = d["k8"].shape[0]
+    ld = (S + 3) // 4 * 4
+    scores = torch.empty((L, ld), dtype=torch.float32, device="cuda")
+    dsa.index(d["q8"], d["q_scale"], d["w"], d["k8"], d["k_scale"], q_pos0=q_pos0, scores=scores)
+    idx = dsa.topk(scores, cfg.k, q_pos0=q_pos0, n_cols=S)
+    _, lse = dsa.sparse_attn(d["q"], d["kv"], idx, cfg.scale)
+    return scores, idx, lse
+
+
+def test_indexer_loss_sparse_config1_all_rows(dsa):
+    cfg = synth.config(1)
+    hinp = synth.prefill_inputs(cfg)
+    d = _cuda(hinp)
+    scores, idx, lse = _gpu_scores_idx_lse(dsa, d, cfg)
+    p, kl, loss = dsa.indexer_loss(d["q"], d["kv"], lse, scores, cfg.scale, idx=idx)
+    assert dsa.device_status() == 0
+    p, kl, idx_h = p.cpu().numpy(), kl.cpu().numpy(), idx.cpu().numpy()
+    total = 0.0
+    for t in range(cfg.L):
+        ref = oracle.indexer_loss_prefill_row(hinp, t, cfg.k, cfg.scale, idx_override=idx_h[t])
+        _check_loss(p[t], kl[t], ref, f"cfg1 row {t}")
+        total += ref["kl"]
+    assert abs(float(loss.item()) - total) <= KL_REL * max(1.0, abs(total))
+
+
+@pytest.mark.parametrize("S,q_pos0,T", [(256, 0, 256), (300, 100, 130)])
+def test_indexer_loss_dense_warmup(dsa, S, q_pos0, T):
+    cfg = synth.config(1, L=S)
+    hinp = synth.prefill_inputs(cfg)
+    d = _cuda(hinp)
+    rows = slice(q_pos0, q_pos0 + T)
+    q8, qs, w, q = (d[n][rows].contiguous() for n in ("q8", "q_scale", "w", "q"))
+    ld = (S + 3) // 4 * 4
+    scores = torch.empty((T, ld), dtype=torch.float32, device="cuda")
+    dsa.index(q8, qs, w, d["k8"], d["k_scale"], q_pos0=q_pos0, scores=scores)
+    _, lse = dsa.dense_causal_attn(q, d["kv"], cfg.scale, q_pos0=q_pos0)
+    p, kl, loss = dsa.indexer_loss(q, d["kv"], lse, scores, cfg.scale, q_pos0=q_pos0)
+    assert p is None and dsa.device_status() == 0
+    kl = kl.cpu().numpy()
+    sub = {n: hinp[n][rows] for n in ("q8", "q_scale", "w", "q")}
+    sub.update({n: hinp[n] for n in ("k8", "k_scale", "kv")})
+    for t in range(T):
+        ref = oracle.indexer_loss_prefill_row(sub, t, cfg.k, cfg.scale, q_pos0=q_pos0, dense=True)
+        _check_loss(None, kl[t], ref, f"dense row {q_pos0 + t}")
+
+
+def test_indexer_loss_4k_sampled_rows_and_range_error(dsa):
+    cfg = synth.config(2)
+    hinp = synth.prefill_inputs(cfg)
+    d = _cuda(hinp)
+    scores, idx, lse = _gpu_scores_idx_lse(dsa, d, cfg)
+    p, kl, _ = dsa.indexer_loss(d["q"], d["kv"], lse, scores, cfg.scale, idx=idx)
+    assert dsa.device_status() == 0
+    rows = [0, 1, 63, 64, 2047, 2048, 3000, 4095]
+    p_h, kl_h, idx_h = p.cpu().numpy(), kl.cpu().numpy(), idx.cpu().numpy()
+    for t in rows:
+        ref = oracle.indexer_loss_prefill_row(hinp, t, cfg.k, cfg.scale, idx_override=idx_h[t])
+        _check_loss(p_h[t], kl_h[t], ref, f"4K row {t}")
+    # a selected position past the score row is skipped and reported
+    last = slice(cfg.L - 8, cfg.L)                       # rows that select positions >= 2048
+    narrow = scores[last, :2048].contiguous()
+    dsa.indexer_loss(d["q"][last].contiguous(), d["kv"], lse[last].contiguous(), narrow, cfg.scale,
+                     idx=idx[last].contiguous())
+    assert dsa.device_status() == 6
+
+
 @pytest.mark.parametrize("n_split", [2, 3, 8])
 def test_attention_key_split_matches_oracle(dsa, n_split):
     g = torch.Generator().manual_seed(21 + n_split)
