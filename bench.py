@@ -277,7 +277,7 @@ def run_ours(args, dist, rank, ws):
     # (profiles/prefill128k_tail_full.md), scaled to the launch's rows; the capture starts from a
     # flushed L2, so it overstates the steady state a little.  None where no capture matches.
     traffic_per_row = {"sparse_attn": (0.424813e9 + 0.116605e9) / 1024, "indexer": (0.063544e9 + 0.475494e9) / 1024,
-                       "topk": (1.015358e9 + 0.007002e9) / 1024}
+                       "topk": (0.61672e9 + 0.0072e9) / 1024}
     traffic = traffic_per_row.get(dom_name)
     if traffic is not None:
         traffic = round(traffic * cfg.L / kern[dom_name]["launches"])

@@ -4,10 +4,12 @@
 // One CTA per row; scores become order-preserving 32-bit keys and the selection is exact.
 //   n <= k         every position is selected.
 //   n <= kCandCap  the row is loaded into shared memory once and selected there.
-//   otherwise      (sample and filter) a strided sample of kSample keys gives a lower bound
-//                  tau that the k-th largest key clears with overwhelming probability: the
-//                  sample's rank-r key, r = the expected sample rank of the k-th largest key
-//                  + 4 standard deviations + 2.  One pass over the row compacts the keys >= tau
+//   otherwise      (sample and filter) a sample of kSample keys (kSample / 4 groups of four
+//                  neighbours at evenly spread positions, one 16-byte load each, so the sample
+//                  touches a quarter of the row's cache lines) gives a lower bound tau that the
+//                  k-th largest key clears with overwhelming probability: the sample's rank-r
+//                  key, r = the expected sample rank of the k-th largest key + 6 standard
+//                  deviations + 2 (the extra margin covers neighbours whose scores correlate).  One pass over the row compacts the keys >= tau
 //                  into shared memory; when between k and kCandCap of them were found, the
 //                  exact selection runs on those.  Otherwise (a sample that missed, or heavy
 //                  ties at tau) the row falls back to a radix select that re-reads it.
@@ -29,6 +31,7 @@ constexpr int kCandCap = 6144;
 constexpr int kSample = 4096;  // held in cand_key until the filter pass starts
 constexpr int kUnroll = 8;     // float4 loads in flight per thread in the filter pass
 static_assert(kSample <= kCandCap, "the sample is staged in the candidate buffer");
+static_assert(kSample % (4 * kThreads) == 0 && kSample <= kCandCap + 1, "sample groups per thread; rows sampled are longer");
 
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
   uint32_t v;
@@ -189,22 +192,31 @@ __device__ void short_row(TopkSmem& s, const float* row, int n, uint32_t k, int3
   select_from_candidates(s, n, k, out);
 }
 
-// The sample's lower bound: kSample keys at evenly spread positions, tau = the sample's rank-r
-// key, returned as a float bound.  {x >= tau_f} is a prefix of the key order for non-NaN x (it
-// takes both zeros or neither), so it holds the row's top k whenever it has k members.
+// The sample's lower bound: kSample keys in groups of four neighbours at evenly spread positions,
+// tau = the sample's rank-r key, returned as a float bound.  {x >= tau_f} is a prefix of the key
+// order for non-NaN x (it takes both zeros or neither), so it holds the row's top k whenever it
+// has k members.  Needs n >= kSample.
 __device__ float sample_bound(TopkSmem& s, const float* row, int n, uint32_t k) {
   const int tid = threadIdx.x;
   {
-    constexpr int kPer = kSample / kThreads;
-    float v[kPer];
+    constexpr int kGroups = kSample / 4, kPer = kGroups / kThreads;
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    const int64_t n4 = n >> 2;
+    float4 v[kPer];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) v[u] = row[static_cast<int64_t>(tid + u * kThreads) * n / kSample];
+    for (int u = 0; u < kPer; ++u) v[u] = row4[static_cast<int64_t>(tid + u * kThreads) * n4 / kGroups];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) s.cand_key[tid + u * kThreads] = order_key(v[u]);
+    for (int u = 0; u < kPer; ++u) {
+      uint32_t* d = s.cand_key + 4 * (tid + u * kThreads);
+      d[0] = order_key(v[u].x);
+      d[1] = order_key(v[u].y);
+      d[2] = order_key(v[u].z);
+      d[3] = order_key(v[u].w);
+    }
   }
   __syncthreads();
   const float mu = static_cast<float>(k) * kSample / n;  // expected sample keys >= the k-th largest
-  uint32_t r = static_cast<uint32_t>(mu + 4.f * sqrtf(mu) + 2.f);
+  uint32_t r = static_cast<uint32_t>(mu + 6.f * sqrtf(mu) + 2.f);
   if (r > kSample) r = kSample;
   uint32_t tau, unused;
   radix_threshold<2>(
@@ -228,7 +240,7 @@ __device__ void filter_range(TopkSmem& s, const float* row, int p0, int p1, floa
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 + u * kThreads;
-      v[u] = i < q1 ? __ldcs(row4 + i) : make_float4(NAN, NAN, NAN, NAN);  // NaN never passes
+      v[u] = i < q1 ? __ldg(row4 + i) : make_float4(NAN, NAN, NAN, NAN);  // NaN never passes
     }
     uint32_t mask = 0;  // bit 4u + c: element c of v[u]
 #pragma unroll
@@ -254,7 +266,7 @@ __device__ void filter_range(TopkSmem& s, const float* row, int p0, int p1, floa
       mask &= mask - 1;
       const int pos = 4 * (i0 + (bit >> 2) * kThreads) + (bit & 3);
       if (base < static_cast<uint32_t>(kCandCap)) {
-        s.cand_key[base] = order_key(row[pos]);  // an L1 hit
+        s.cand_key[base] = order_key(row[pos]);  // an L1 hit: the loads above were cached
         s.cand_pos[base] = pos;
       }
       ++base;

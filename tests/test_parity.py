@@ -174,6 +174,13 @@ def _topk_valid(vals, sel, k):
     assert np.isin(strict, sel).all()
 
 
+def _sample_grid(n):
+    """Positions the top-k kernel's bound estimate reads in a row of n > 6144 keys: 1024 groups of
+    four neighbours starting at 4 * floor(g * floor(n / 4) / 1024)."""
+    g = 4 * ((np.arange(1024) * (n // 4)) // 1024)
+    return (g[:, None] + np.arange(4)).ravel()
+
+
 @pytest.mark.parametrize("dist", ["normal", "ties", "const", "lognormal", "negative", "tiny_range", "spikes"])
 @pytest.mark.parametrize("n,k", [(100, 64), (2049, 2048), (4097, 2048), (6144, 2048), (6145, 2048),
                                  (131072, 2048), (70000, 64), (3000, 1)])
@@ -191,10 +198,10 @@ def test_topk_exact_on_fixed_scores(dsa, dist, n, k):
     elif dist == "negative":
         v = -np.abs(rng.standard_normal((T, n))) * 1e3
     elif dist == "spikes":
-        # large values on an evenly strided grid of 4096 positions, small ones elsewhere:
-        # a strided sample of the row sees only the spikes
+        # large values on the 1024 evenly spread groups of four neighbours that the kernel's
+        # sample reads, small ones elsewhere: the sample sees only the spikes (the fallback path)
         v = rng.random((T, n))
-        v[:, (np.arange(4096) * n) // 4096] += 100.0
+        v[:, _sample_grid(n)] += 100.0
     else:
         v = 1.0 + rng.integers(0, 50, (T, n)) * 2.0 ** -23
     v = v.astype(np.float32)
@@ -225,7 +232,7 @@ def test_topk_many_long_rows(dsa, dist):
         v = np.full((T, n), -2.5)
     else:
         v = rng.random((T, n))
-        v[:, (np.arange(4096) * n) // 4096] += 100.0
+        v[:, _sample_grid(n)] += 100.0
     v = v.astype(np.float32)
     lens = torch.tensor([n - 7 * t for t in range(T)], dtype=torch.int32)
     idx = dsa.topk(torch.from_numpy(v).cuda(), k, row_lens=lens.cuda()).cpu().numpy()
