@@ -592,6 +592,14 @@ __device__ __forceinline__ void attn_body(const AttnArgs& a, const CUtensorMap* 
           for (int b = 0; b < 9; ++b)
             ptx::tma_load_2d_hint(sbase + kOffK + b * kQBoxBytes, qmap, baddr(bars.q_full), b * 64, it.t * a.H,
                                   ptx::l2_evict_first_policy());  // Q and O stream: keep L2 for latent rows
+          // the next item's Q (work items are dealt round-robin) into L2, so that its load after this
+          // item's last product is an L2 hit
+          const int64_t next_id = cl + static_cast<int64_t>(j + 1) * n_cl;
+          if (next_id < static_cast<int64_t>(a.T) * a.n_split) {
+            const int nt = static_cast<int>(next_id / a.n_split);
+#pragma unroll 1
+            for (int b = 0; b < 9; ++b) ptx::tma_prefetch_2d(qmap, b * 64, nt * a.H);
+          }
         }
         __syncwarp();
         q_last = nq;

@@ -546,6 +546,42 @@ def test_forward_prefill_config4_full_size_sampled_rows(dsa):
         _check_attention(f.out[t].float().cpu().numpy(), f.lse[t].cpu().numpy(), o_ref, lse_ref, f"cfg4 row {t}")
 
 
+def test_full_size_128k_dense_attention_and_indexer_loss_sampled_rows(dsa):
+    """The 128K workload at full size for the dense causal attention (one launch over all rows, as
+    the length curve runs it) and for the indexer loss of both stages on the last 8192-row chunk
+    (as the training-side bench runs it); sampled rows against the oracle."""
+    cfg = synth.config(4)
+    L = cfg.L
+    d = synth.prefill_inputs(cfg, device="cuda")
+    out, lse_dense = dsa.dense_causal_attn(d["q"], d["kv"], cfg.scale)
+    assert dsa.device_status() == 0
+    keys = {n: d[n].cpu() for n in ("k8", "k_scale", "kv")}
+    for t in [0, 4095, 65536, L - 1]:
+        o_ref, l_ref = oracle.dense_causal_row(d["q"][t].cpu(), keys["kv"], t, cfg.scale)
+        _check_attention(out[t].float().cpu().numpy(), lse_dense[t].cpu().numpy(), o_ref, l_ref, f"dense 128K row {t}")
+    del out
+    torch.cuda.empty_cache()
+    r0, T = L - 8192, 8192
+    rows = slice(r0, L)
+    ld = (L + 3) // 4 * 4
+    scores = torch.empty((T, ld), dtype=torch.float32, device="cuda")
+    dsa.index(d["q8"][rows], d["q_scale"][rows], d["w"][rows], d["k8"], d["k_scale"], q_pos0=r0, scores=scores)
+    idx = dsa.topk(scores, cfg.k, q_pos0=r0, n_cols=L)
+    q = d["q"][rows]
+    _, lse = dsa.sparse_attn(q, d["kv"], idx, cfg.scale)
+    p, kl, _ = dsa.indexer_loss(q, d["kv"], lse, scores, cfg.scale, idx=idx)
+    _, kl_dense, _ = dsa.indexer_loss(q, d["kv"], lse_dense[rows].contiguous(), scores, cfg.scale, q_pos0=r0)
+    assert dsa.device_status() == 0
+    p, kl, kl_dense, idx_h = p.cpu().numpy(), kl.cpu().numpy(), kl_dense.cpu().numpy(), idx.cpu().numpy()
+    for i in [0, 4000, T - 1]:
+        t = r0 + i
+        row_inp = dict(keys, **{n: {t: d[n][t].cpu()} for n in ("q8", "q_scale", "w", "q")})
+        ref = oracle.indexer_loss_prefill_row(row_inp, t, cfg.k, cfg.scale, idx_override=idx_h[i])
+        _check_loss(p[i], kl[i], ref, f"loss 128K row {t}")
+        ref_d = oracle.indexer_loss_prefill_row(row_inp, t, cfg.k, cfg.scale, dense=True)
+        _check_loss(None, kl_dense[i], ref_d, f"dense loss 128K row {t}")
+
+
 # ----------------------------------------------------------------------------- failure path
 
 
