@@ -426,73 +426,66 @@ def bench_dense_curve(dsa, synth, args, peaks, lengths=(4096, 16384, 32768, 6553
 
 
 def bench_indexer_loss(dsa, synth, args, peaks, dense_L=32768):
-    """Training-side forward of the 128K prefill: per 8192-row chunk the indexer, top-k, sparse
-    attention (for lse) and the indexer's KL loss over the selected sets; plus the dense warm-up
-    stage (indexer, dense causal attention, KL over every preceding key) on a 32K sequence."""
+    """Training-side forward of the 128K prefill through dsa_forward_loss (per 8192-row chunk: the
+    indexer, top-k, sparse attention for lse and the indexer's KL loss over the selected sets); plus
+    the dense warm-up stage (indexer, dense causal attention, KL over every preceding key) on a 32K
+    sequence.  The loss kernel's own time comes from a second pass that makes the same launches one
+    by one with CUDA events around the loss launches."""
     out = {}
     for stage, L in (("sparse", 131072), ("dense_warmup", dense_L)):
         cfg = synth.config(4, L=L)
         d = synth.prefill_inputs(cfg, device="cuda")
         chunk = min(args.chunk, L)
-        ld = (L + 3) // 4 * 4
-        scores = torch.empty((chunk, ld), dtype=torch.float32, device="cuda")
-        idx = torch.empty((L, cfg.k), dtype=torch.int32, device="cuda")
-        o = torch.empty((L, cfg.H, 512), dtype=torch.bfloat16, device="cuda")
-        lse = torch.empty((L, cfg.H), dtype=torch.float32, device="cuda")
-        kl = torch.empty((L,), dtype=torch.float32, device="cuda")
-        p = torch.empty((chunk, cfg.k), dtype=torch.float32, device="cuda")
-        loss = torch.zeros((1,), dtype=torch.float64, device="cuda")
-        n_chunks = (L + chunk - 1) // chunk
-
-        def step(ev=None):
-            loss.zero_()
-            for c in range(n_chunks):
-                r0, r1 = c * chunk, min(L, (c + 1) * chunk)
-                sc = scores[: r1 - r0]
-                dsa.index(d["q8"][r0:r1], d["q_scale"][r0:r1], d["w"][r0:r1], d["k8"], d["k_scale"], q_pos0=r0,
-                          scores=sc)
-                if stage == "sparse":
-                    dsa.topk(sc, cfg.k, q_pos0=r0, n_cols=L, idx=idx[r0:r1])
-                    dsa.sparse_attn(d["q"][r0:r1], d["kv"], idx[r0:r1], cfg.scale, out=o[r0:r1], lse=lse[r0:r1])
-                else:
-                    dsa.dense_causal_attn(d["q"][r0:r1], d["kv"], cfg.scale, q_pos0=r0, out=o[r0:r1], lse=lse[r0:r1])
-                if ev is not None:
-                    ev.append(_rec())
-                if stage == "sparse":
-                    dsa.indexer_loss(d["q"][r0:r1], d["kv"], lse[r0:r1], sc, cfg.scale, idx=idx[r0:r1],
-                                     p=p[: r1 - r0], kl=kl[r0:r1], loss=loss)
-                else:
-                    dsa.indexer_loss(d["q"][r0:r1], d["kv"], lse[r0:r1], sc, cfg.scale, q_pos0=r0, kl=kl[r0:r1],
-                                     loss=loss)
-                if ev is not None:
-                    ev.append(_rec())
-
+        sparse = stage == "sparse"
+        idx = torch.empty((L, cfg.k), dtype=torch.int32, device="cuda") if sparse else None
+        f = dsa.ForwardLoss(d, cfg.k, cfg.scale, stage=dsa.LOSS_SPARSE if sparse else dsa.LOSS_DENSE_WARMUP,
+                            chunk_rows=chunk, idx=idx)
         for _ in range(args.warmup):
-            step()
+            f()
         torch.cuda.synchronize()
         n = max(2, min(args.steps, 3))
-        ev = []
         a = _rec()
         for _ in range(n):
-            step(ev)
+            f()
         b = _rec()
         b.synchronize()
+        ms = a.elapsed_time(b) / n
+        loss_value = float(f.loss.item())
+        # breakdown: the same launches one by one, events around the loss launches
+        ld = (L + 3) // 4 * 4
+        scores = torch.empty((chunk, ld), dtype=torch.float32, device="cuda")
+        loss = torch.zeros((1,), dtype=torch.float64, device="cuda")
+        ev = []
+        for c in range((L + chunk - 1) // chunk):
+            r0, r1 = c * chunk, min(L, (c + 1) * chunk)
+            sc = scores[: r1 - r0]
+            dsa.index(d["q8"][r0:r1], d["q_scale"][r0:r1], d["w"][r0:r1], d["k8"], d["k_scale"], q_pos0=r0, scores=sc)
+            if sparse:
+                dsa.topk(sc, cfg.k, q_pos0=r0, n_cols=L, idx=idx[r0:r1])
+                dsa.sparse_attn(d["q"][r0:r1], d["kv"], idx[r0:r1], cfg.scale, out=f.out[r0:r1], lse=f.lse[r0:r1])
+            else:
+                dsa.dense_causal_attn(d["q"][r0:r1], d["kv"], cfg.scale, q_pos0=r0, out=f.out[r0:r1], lse=f.lse[r0:r1])
+            ev.append(_rec())
+            dsa.indexer_loss(d["q"][r0:r1], d["kv"], f.lse[r0:r1], sc, cfg.scale, idx=idx[r0:r1] if sparse else None,
+                             q_pos0=0 if sparse else r0, want_p=False, kl=f.kl[r0:r1], loss=loss)
+            ev.append(_rec())
+        torch.cuda.synchronize()
         st = dsa.device_status()
         if st != 0:
             raise RuntimeError(f"device status {st} ({stage})")
-        ms = a.elapsed_time(b) / n
-        loss_ms = _pairs_ms(ev) / n
+        loss_ms = _pairs_ms(ev)
         pairs = (sum(min(t + 1, cfg.k) for t in range(min(L, cfg.k))) + max(0, L - cfg.k) * cfg.k
-                 if stage == "sparse" else L * (L + 1) // 2)
+                 if sparse else L * (L + 1) // 2)
         flop = 2.0 * cfg.H * 576 * pairs
         tf = flop / (loss_ms * 1e-3) / 1e12
         out[stage] = {"L": L, "step_ms": round(ms, 3), "tokens_per_s": round(L / (ms * 1e-3), 1),
-                      "loss_kernel_ms": round(loss_ms, 3), "loss_launches": n_chunks,
+                      "path": "dsa_forward_loss (C ABI)",
+                      "loss_kernel_ms": round(loss_ms, 3), "loss_launches": len(ev) // 2,
                       "loss_kernel": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_sus"],
                                       "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_sus"], 4),
                                       "work": "2 H 576 FLOP per (row, key) pair of the set (QK^T recomputed)"},
-                      "loss_value": float(loss.item())}
-        del d, scores, idx, o, lse, kl, p
+                      "loss_value": loss_value, "loss_value_breakdown_pass": float(loss.item())}
+        del d, scores, f, idx
         torch.cuda.empty_cache()
     sp = out["sparse"]
     return {"metric": "training-side prefill tokens/s with the indexer KL loss (128K, sparse stage)",

@@ -282,6 +282,30 @@ size_t dsa_forward_workspace_size(const dsa_forward_args* args);
 dsa_status_t dsa_forward(const dsa_forward_args* args, void* ws, size_t ws_bytes,
                          dsa_stream_t stream);
 
+/* Stages of the indexer's training loss (freezhihu.org/question/1978819912970555965 §2.3). */
+enum { DSA_LOSS_SPARSE = 0, DSA_LOSS_DENSE_WARMUP = 1 };
+
+/* Bytes of device workspace dsa_forward_loss needs (0 on invalid args). */
+size_t dsa_forward_loss_workspace_size(const dsa_forward_args* args, int stage);
+
+/*
+ * dsa_forward_loss — the training-side prefill forward with the indexer's loss
+ * (§2.3.2 sparse stage, §2.3.1 dense warm-up).  args as for dsa_forward with
+ * mode = DSA_MODE_PREFILL; args->lse is required (it feeds the loss).  For each chunk of
+ * chunk_rows query rows (0 = library choice):
+ *   DSA_LOSS_SPARSE:       dsa_index, dsa_topk, dsa_sparse_attn over the chunk's selection,
+ *                          then dsa_indexer_loss over the same selection;
+ *   DSA_LOSS_DENSE_WARMUP: dsa_index, dsa_dense_causal_attn (every preceding key), then
+ *                          dsa_indexer_loss over every preceding key (args->idx and k unused
+ *                          beyond validation).
+ * Outputs: out, lse, idx (sparse stage, when non-NULL) as for dsa_forward; kl [T] per-row KL
+ * terms (device, or NULL); *loss_acc (one device double, or NULL) has sum_t KL_t ADDED to it.
+ * `ws`: dsa_forward_loss_workspace_size(args, stage) bytes, 256-byte aligned (the fp32 score
+ * block of one chunk, and the selection when args->idx is NULL).  Errors as dsa_forward.
+ */
+dsa_status_t dsa_forward_loss(const dsa_forward_args* args, int stage, float* kl, double* loss_acc, void* ws,
+                              size_t ws_bytes, dsa_stream_t stream);
+
 /*
  * dsa_prefill_host — the prefill forward (mode DSA_MODE_PREFILL of dsa_forward) with every
  * tensor in HOST memory: args->q8, q_scale, w, k8, k_scale, q, kv and the outputs out, lse

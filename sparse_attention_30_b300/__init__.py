@@ -25,7 +25,8 @@ EXPORTS = ("dsa_status_string", "dsa_version", "dsa_index", "dsa_index_paged", "
            "dsa_forward_workspace_size", "dsa_forward", "dsa_device_status", "dsa_selftest_wait_timeout",
            "dsa_decode_noalloc", "dsa_decode_noalloc_capacity", "dsa_sparse_attn_split_workspace_size",
            "dsa_sparse_attn_split", "dsa_prefill_host_workspace_size", "dsa_prefill_host",
-           "dsa_dense_causal_attn", "dsa_indexer_loss", "dsa_wait_limit_ns")
+           "dsa_dense_causal_attn", "dsa_indexer_loss", "dsa_wait_limit_ns", "dsa_forward_loss_workspace_size",
+           "dsa_forward_loss")
 
 
 class DSAError(RuntimeError):
@@ -78,6 +79,8 @@ def _load():
         "dsa_indexer_loss": ([P, P, I64, P, I, I, I, I64, F, P, P, I64, P, P, P, P], I),
         "dsa_sparse_attn_split": ([P, P, I64, P, I64, I, P, I, I, I, F, P, P, I, P, ctypes.c_size_t, P], I),
         "dsa_prefill_host_workspace_size": ([ctypes.POINTER(ForwardArgs)], ctypes.c_size_t),
+        "dsa_forward_loss_workspace_size": ([ctypes.POINTER(ForwardArgs), I], ctypes.c_size_t),
+        "dsa_forward_loss": ([ctypes.POINTER(ForwardArgs), I, P, P, P, ctypes.c_size_t, P], I),
         "dsa_prefill_host": ([ctypes.POINTER(ForwardArgs), P, ctypes.c_size_t, P], I),
     }
     for name, (args, res) in sig.items():
@@ -304,6 +307,48 @@ class Forward:
         s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(self.out)
         _check(lib.dsa_forward(ctypes.byref(self.args), _ptr(self.ws), self.ws.numel(), s), "dsa_forward")
         return self.out
+
+
+LOSS_SPARSE, LOSS_DENSE_WARMUP = 0, 1
+
+
+class ForwardLoss:
+    """Training-side prefill forward with the indexer's KL loss (dsa_forward_loss): owns the workspace.
+
+    ForwardLoss(inputs, k, scale, stage) with inputs = dict(q8, q_scale, w, k8, k_scale, q, kv) on the GPU and
+    stage LOSS_SPARSE (selected sets) or LOSS_DENSE_WARMUP (every preceding key).  Calling it writes self.out,
+    self.lse, self.kl (and self.idx in the sparse stage when given) and returns self.loss, a float64 tensor
+    of one element holding sum_t KL_t of this call.
+    """
+
+    def __init__(self, inp, k, scale, stage=LOSS_SPARSE, q_pos0=0, chunk_rows=0, idx=None):
+        q8 = inp["q8"]
+        T, H_I, _ = q8.shape
+        H = inp["q"].shape[1]
+        dev = q8.device
+        self.stage = stage
+        self.out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        self.kl = torch.empty((T,), dtype=torch.float32, device=dev)
+        self.loss = torch.zeros((1,), dtype=torch.float64, device=dev)
+        self.idx = idx
+        self.args = ForwardArgs(mode=MODE_PREFILL, H_I=H_I, H=H, k=k, scale=scale, T=T, S=inp["k8"].shape[0],
+                                q_pos0=q_pos0, chunk_rows=chunk_rows,
+                                q8=_ptr(q8), q_scale=_ptr(inp["q_scale"]), w=_ptr(inp["w"]), k8=_ptr(inp["k8"]),
+                                k_scale=_ptr(inp["k_scale"]), q=_ptr(inp["q"]), kv=_ptr(inp["kv"]),
+                                out=_ptr(self.out), lse=_ptr(self.lse), idx=_ptr(idx))
+        self._keep = inp
+        n = lib.dsa_forward_loss_workspace_size(ctypes.byref(self.args), stage)
+        if n == 0:
+            raise DSAError(1, "dsa_forward_loss_workspace_size")
+        self.ws = torch.empty(n, dtype=torch.uint8, device=dev)
+
+    def __call__(self, stream=None):
+        s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(self.out)
+        self.loss.zero_()
+        _check(lib.dsa_forward_loss(ctypes.byref(self.args), self.stage, _ptr(self.kl), _ptr(self.loss), _ptr(self.ws),
+                                    self.ws.numel(), s), "dsa_forward_loss")
+        return self.loss
 
 
 class PrefillHost:

@@ -466,6 +466,67 @@ dsa_status_t dsa_forward(const dsa_forward_args* a, void* ws, size_t ws_bytes, d
                            p.n_split > 1 ? reinterpret_cast<float*>(part + p.part_o_bytes) : nullptr, s);
 }
 
+size_t dsa_forward_loss_workspace_size(const dsa_forward_args* args, int stage) {
+  FwdPlan p;
+  if (!args || args->mode != DSA_MODE_PREFILL || (stage != DSA_LOSS_SPARSE && stage != DSA_LOSS_DENSE_WARMUP) ||
+      plan_forward(args, &p) != DSA_OK)
+    return 0;
+  return stage == DSA_LOSS_SPARSE ? p.total : p.scores_bytes;
+}
+
+dsa_status_t dsa_forward_loss(const dsa_forward_args* a, int stage, float* kl, double* loss_acc, void* ws,
+                              size_t ws_bytes, dsa_stream_t stream) {
+  if (!a || a->mode != DSA_MODE_PREFILL || (stage != DSA_LOSS_SPARSE && stage != DSA_LOSS_DENSE_WARMUP))
+    return DSA_ERR_INVALID_ARG;
+  FwdPlan p;
+  dsa_status_t st = plan_forward(a, &p);
+  if (st != DSA_OK) return st;
+  if (!a->q8 || !a->q_scale || !a->w || !a->k8 || !a->k_scale || !a->q || !a->kv || !a->out || !a->lse)
+    return DSA_ERR_INVALID_ARG;
+  if (p.rows == 0) return DSA_OK;
+  const bool sparse = stage == DSA_LOSS_SPARSE;
+  const size_t need = sparse ? p.total : p.scores_bytes;
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
+  float* scores = static_cast<float*>(ws);
+  int32_t* idx = !sparse ? nullptr
+                         : a->idx ? a->idx : reinterpret_cast<int32_t*>(static_cast<char*>(ws) + p.scores_bytes);
+  st = check_index_args(a->q8, a->q_scale, a->w, a->k8, a->k_scale, a->T, a->S, a->H_I, a->q_pos0, scores, p.ld);
+  if (st != DSA_OK) return st;
+  if (sparse) {
+    st = check_attn_args(a->q, a->kv, a->S, nullptr, 0, 0, idx, a->T, a->H, a->k, a->out);
+    if (st != DSA_OK) return st;
+  }
+  cudaStream_t s = stream;
+  for (int r0 = 0; r0 < a->T; r0 += p.chunk) {
+    const int rows = std::min(p.chunk, a->T - r0);
+    const int64_t pos0 = a->q_pos0 + r0;
+    const uint16_t* q = a->q + static_cast<int64_t>(r0) * a->H * 576;
+    uint16_t* out = a->out + static_cast<int64_t>(r0) * a->H * 512;
+    float* lse = a->lse + static_cast<int64_t>(r0) * a->H;
+    float* kl_c = kl ? kl + r0 : nullptr;
+    st = dsa_index(a->q8 + static_cast<int64_t>(r0) * a->H_I * 128, a->q_scale + static_cast<int64_t>(r0) * a->H_I,
+                   a->w + static_cast<int64_t>(r0) * a->H_I, a->k8, a->k_scale, rows, a->S, a->H_I, pos0, scores,
+                   p.ld, s);
+    if (st != DSA_OK) return st;
+    if (sparse) {
+      int32_t* idx_c = idx + static_cast<int64_t>(r0) * a->k;
+      st = dsa_topk(scores, p.ld, rows, nullptr, a->S, pos0, a->k, idx_c, s);
+      if (st != DSA_OK) return st;
+      st = dsa_sparse_attn(q, a->kv, a->S, nullptr, 0, 0, idx_c, rows, a->H, a->k, a->scale, out, lse, s);
+      if (st != DSA_OK) return st;
+      st = dsa_indexer_loss(q, a->kv, a->S, idx_c, rows, a->H, a->k, 0, a->scale, lse, scores, p.ld, nullptr, kl_c,
+                            loss_acc, s);
+    } else {
+      st = dsa_dense_causal_attn(q, a->kv, a->S, rows, a->H, pos0, a->scale, out, lse, s);
+      if (st != DSA_OK) return st;
+      st = dsa_indexer_loss(q, a->kv, a->S, nullptr, rows, a->H, 0, pos0, a->scale, lse, scores, p.ld, nullptr, kl_c,
+                            loss_acc, s);
+    }
+    if (st != DSA_OK) return st;
+  }
+  return DSA_OK;
+}
+
 size_t dsa_prefill_host_workspace_size(const dsa_forward_args* args) {
   HostPlan h;
   if (plan_prefill_host(args, &h) != DSA_OK) return 0;

@@ -1042,19 +1042,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (log2 domain), sum l_s and normalised output O_s, the row's softmax weights over the union of the
 // splits give O = sum_s l_s 2^(m_s - m) O_s / sum_s l_s 2^(m_s - m), m = max_s m_s.
 __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
+  constexpr int kMaxSplit = 8;
   const int t = blockIdx.x / a.H, h = blockIdx.x % a.H;
   const int64_t base = static_cast<int64_t>(t) * a.n_split * a.H + h;
+  // every load is issued before any is used (one memory round trip, not two)
+  float ms[kMaxSplit], ls[kMaxSplit];
+  float4 o[kMaxSplit];
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) {
+    if (s < a.n_split) {
+      const int64_t r = base + static_cast<int64_t>(s) * a.H;
+      const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[r];
+      ms[s] = ml.x;
+      ls[s] = ml.y;
+      o[s] = reinterpret_cast<const float4*>(a.part_o + r * kDV)[threadIdx.x];
+    }
+  }
   float m = -INFINITY;
-  for (int s = 0; s < a.n_split; ++s) m = fmaxf(m, a.part_ml[(base + static_cast<int64_t>(s) * a.H) * 2]);
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s)
+    if (s < a.n_split) m = fmaxf(m, ms[s]);
   float wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < a.n_split; ++s) {
-    const int64_t r = base + static_cast<int64_t>(s) * a.H;
-    const float ms = a.part_ml[r * 2], ls = a.part_ml[r * 2 + 1];
-    const float wt = (ls > 0.f && m > -INFINITY) ? ls * fast_exp2(ms - m) : 0.f;
-    const float4 o = reinterpret_cast<const float4*>(a.part_o + r * kDV)[threadIdx.x];
-    acc.x += wt * o.x; acc.y += wt * o.y; acc.z += wt * o.z; acc.w += wt * o.w;
-    wsum += wt;
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) {
+    if (s < a.n_split) {
+      const float wt = (ls[s] > 0.f && m > -INFINITY) ? ls[s] * fast_exp2(ms[s] - m) : 0.f;
+      acc.x += wt * o[s].x; acc.y += wt * o[s].y; acc.z += wt * o[s].z; acc.w += wt * o[s].w;
+      wsum += wt;
+    }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   uint2 pk;

@@ -163,6 +163,26 @@ def test_forward_workspace_and_validation():
     assert dsa.lib.dsa_forward(ctypes.byref(d), None, 0, None) == 1
 
 
+def test_forward_loss_workspace_and_validation():
+    dsa = _lib()
+    a = dsa.ForwardArgs(mode=dsa.MODE_PREFILL, H_I=64, H=128, k=2048, scale=0.07, T=4096, S=4096, q_pos0=0,
+                        chunk_rows=1024)
+    ws = dsa.lib.dsa_forward_loss_workspace_size
+    # sparse stage: the score block of one chunk plus the selection of all rows (as dsa_forward)
+    assert ws(ctypes.byref(a), dsa.LOSS_SPARSE) == 1024 * 4096 * 4 + 4096 * 2048 * 4
+    # dense warm-up: the score block only
+    assert ws(ctypes.byref(a), dsa.LOSS_DENSE_WARMUP) == 1024 * 4096 * 4
+    assert ws(ctypes.byref(a), 2) == 0                                   # no such stage
+    d = dsa.ForwardArgs(mode=dsa.MODE_DECODE, H_I=64, H=128, k=2048, scale=0.07, B=64, page_size=64,
+                        n_pages=32768, bt_stride=512, max_seq_len=32768)
+    assert ws(ctypes.byref(d), dsa.LOSS_SPARSE) == 0                     # prefill only
+    f = dsa.lib.dsa_forward_loss
+    assert f(ctypes.byref(d), dsa.LOSS_SPARSE, None, None, None, 0, None) == 1
+    assert f(ctypes.byref(a), 5, None, None, None, 0, None) == 1
+    # every input and lse are required (lse feeds the loss), checked before the workspace
+    assert f(ctypes.byref(a), dsa.LOSS_SPARSE, None, None, None, 0, None) == 1
+
+
 def test_prefill_host_workspace_and_validation():
     dsa = _lib()
     a = dsa.ForwardArgs(mode=dsa.MODE_PREFILL, H_I=64, H=128, k=2048, scale=0.07, T=4096, S=4096, q_pos0=0,

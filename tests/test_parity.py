@@ -418,6 +418,38 @@ def test_indexer_loss_4k_sampled_rows_and_range_error(dsa):
     assert dsa.device_status() == 6
 
 
+@pytest.mark.parametrize("stage", [0, 1])
+def test_forward_loss_matches_the_separate_calls(dsa, stage):
+    # dsa_forward_loss on the 4K workload in 1024-row chunks against the same kernels called one by one
+    cfg = synth.config(2)
+    d = synth.prefill_inputs(cfg, device="cuda")
+    f = dsa.ForwardLoss(d, cfg.k, cfg.scale, stage=stage, chunk_rows=1024,
+                        idx=torch.empty((cfg.L, cfg.k), dtype=torch.int32, device="cuda") if stage == 0 else None)
+    loss = f().item()
+    assert dsa.device_status() == 0
+    kl_ref = torch.empty(cfg.L, device="cuda")
+    ld = cfg.L
+    scores = torch.empty((1024, ld), dtype=torch.float32, device="cuda")
+    for r0 in range(0, cfg.L, 1024):
+        rows = slice(r0, r0 + 1024)
+        dsa.index(d["q8"][rows], d["q_scale"][rows], d["w"][rows], d["k8"], d["k_scale"], q_pos0=r0, scores=scores)
+        q = d["q"][rows]
+        if stage == 0:
+            idx = dsa.topk(scores, cfg.k, q_pos0=r0, n_cols=cfg.L)
+            assert torch.equal(torch.sort(idx, dim=1).values, torch.sort(f.idx[rows], dim=1).values)
+            out, lse = dsa.sparse_attn(q, d["kv"], idx, cfg.scale)
+            dsa.indexer_loss(q, d["kv"], lse, scores, cfg.scale, idx=idx, want_p=False, kl=kl_ref[rows])
+        else:
+            out, lse = dsa.dense_causal_attn(q, d["kv"], cfg.scale, q_pos0=r0)
+            dsa.indexer_loss(q, d["kv"], lse, scores, cfg.scale, q_pos0=r0, kl=kl_ref[rows])
+        # the same kernels on the same inputs: equal up to the order of equal-score selections
+        assert (out.float() - f.out[rows].float()).abs().max().item() <= MAX_TOL
+        assert (lse - f.lse[rows]).abs().max().item() <= 1e-4
+    assert dsa.device_status() == 0
+    np.testing.assert_allclose(f.kl.cpu().numpy(), kl_ref.cpu().numpy(), rtol=1e-5, atol=1e-6)
+    assert abs(loss - kl_ref.double().sum().item()) <= 1e-5 * max(1.0, abs(loss))
+
+
 @pytest.mark.parametrize("n_split", [2, 3, 8])
 def test_attention_key_split_matches_oracle(dsa, n_split):
     g = torch.Generator().manual_seed(21 + n_split)
