@@ -276,8 +276,8 @@ def run_ours(args, dist, rank, ws):
     # DRAM bytes (read + write) per query row from the ncu capture of the 1024-row 128K tail
     # (profiles/prefill128k_tail_full.md), scaled to the launch's rows; the capture starts from a
     # flushed L2, so it overstates the steady state a little.  None where no capture matches.
-    traffic_per_row = {"sparse_attn": (0.424813e9 + 0.116605e9) / 1024, "indexer": (0.063544e9 + 0.475494e9) / 1024,
-                       "topk": (0.61672e9 + 0.0072e9) / 1024}
+    traffic_per_row = {"sparse_attn": (0.496003e9 + 0.116915e9) / 1024, "indexer": (0.06382e9 + 0.475909e9) / 1024,
+                       "topk": (0.617335e9 + 0.007506e9) / 1024}
     traffic = traffic_per_row.get(dom_name)
     if traffic is not None:
         traffic = round(traffic * cfg.L / kern[dom_name]["launches"])
