@@ -71,7 +71,9 @@ def _check_row(hinp, t, k, scale, idx_row, o_row, lse_row, q_pos0=0, decode=Fals
     else:
         kv = hinp["kv"]
         assert use.max() <= q_pos0 + t
-    o_ref, lse_ref = oracle.attention_row(hinp["q"][t], kv[torch.as_tensor(use)], scale)
+    # index with an integer array (a one-element torch tensor would index a NumPy array as a scalar)
+    sel = kv[np.asarray(use, dtype=np.int64)] if isinstance(kv, np.ndarray) else kv[torch.as_tensor(use, dtype=torch.long)]
+    o_ref, lse_ref = oracle.attention_row(hinp["q"][t], sel, scale)
     _check_attention(o_row, lse_row, o_ref, lse_ref, f"{where} row {t}")
     return nswap
 
@@ -612,6 +614,64 @@ def test_full_size_128k_dense_attention_and_indexer_loss_sampled_rows(dsa):
         _check_loss(p[i], kl[i], ref, f"loss 128K row {t}")
         ref_d = oracle.indexer_loss_prefill_row(row_inp, t, cfg.k, cfg.scale, dense=True)
         _check_loss(None, kl_dense[i], ref_d, f"dense loss 128K row {t}")
+
+
+# ----------------------------------------------------------------------------- shape sweep
+
+_PREFILL_SWEEP = [  # (L, H_I, H, k, chunk_rows, q_pos0): one head, k = 1, one-token sequences, odd chunks
+    (1, 8, 1, 1, 0, 0),
+    (2, 16, 3, 1, 1, 0),
+    (65, 32, 17, 7, 7, 0),
+    (300, 64, 100, 64, 128, 0),
+    (1000, 128, 128, 100, 333, 0),
+    (700, 64, 64, 2048, 0, 0),          # k above every row's length: whole prefixes
+    (513, 16, 128, 64, 100, 257),       # a chunk of rows starting at position 257
+]
+
+
+@pytest.mark.parametrize("L,H_I,H,k,chunk,q_pos0", _PREFILL_SWEEP)
+def test_forward_prefill_shape_sweep(dsa, L, H_I, H, k, chunk, q_pos0):
+    cfg = synth.config(1, L=L, H_I=H_I, H=H, k=k, planted=min(8, L), seed=L + H)
+    full = synth.prefill_inputs(cfg)
+    rows = slice(q_pos0, L)
+    hinp = {n: (full[n][rows].contiguous() if n in ("q8", "q_scale", "w", "q") else full[n]) for n in full}
+    T = L - q_pos0
+    d = _cuda(hinp)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    f = dsa.Forward.prefill(d, k, cfg.scale, q_pos0=q_pos0, chunk_rows=chunk, lse=lse, idx=idx)
+    f()
+    assert dsa.device_status() == 0
+    idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
+    check = range(T) if T * H <= 8192 else sorted({0, 1, T // 3, T // 2, T - 2, T - 1})
+    for t in check:
+        assert np.all(idx[t, min(k, q_pos0 + t + 1):] == -1)
+        _check_row(hinp, t, k, cfg.scale, idx[t], out[t], lse[t], q_pos0=q_pos0, where=f"sweep L={L} H={H} k={k}")
+
+
+_DECODE_SWEEP = [  # (B, H_I, H, k, page, ctx_lo, ctx_hi); the paged indexer takes H_I = 64 or 128
+    (1, 64, 1, 1, 16, 1, 1),            # one sequence of one token
+    (3, 128, 5, 7, 16, 1, 200),
+    (75, 64, 128, 64, 64, 64, 3000),    # more sequences than SM pairs: no key split
+    (5, 128, 128, 2048, 64, 100, 5000),  # key split over few sequences, rows shorter than k
+]
+
+
+@pytest.mark.parametrize("B,H_I,H,k,page,lo,hi", _DECODE_SWEEP)
+def test_forward_decode_shape_sweep(dsa, B, H_I, H, k, page, lo, hi):
+    cfg = synth.config(5, B=B, H_I=H_I, H=H, k=k, page=page, ctx_lo=lo, ctx_hi=hi, planted=min(4, lo - 1) if lo > 1 else 0,
+                       seed=B * 7 + H)
+    hinp = synth.decode_inputs(cfg)
+    d = _cuda(hinp)
+    max_len = int(hinp["seq_lens"].max())
+    idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    f = dsa.Forward.decode(d, k, cfg.scale, max_len, lse=lse, idx=idx)
+    f()
+    assert dsa.device_status() == 0
+    idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
+    for b in sorted({0, B // 2, B - 1}):
+        _check_row(hinp, b, k, cfg.scale, idx[b], out[b], lse[b], decode=True, where=f"decode sweep B={B} H={H} k={k}")
 
 
 # ----------------------------------------------------------------------------- failure path
