@@ -100,6 +100,7 @@ dsa_status_t dsa_index(const uint8_t* q8, const float* q_scale, const float* w,
  *   scores        [B, ld] fp32, ld >= max_seq_len, ld % 4 == 0
  *   page_size must divide 128 and be a multiple of 8; n_pages bounds the page numbers
  *   (an out-of-range page number is skipped and reported as DSA_ERR_DEVICE_RANGE).
+ *   H_I must be 32, 64 or 128 (other head counts return DSA_ERR_UNSUPPORTED).
  */
 dsa_status_t dsa_index_paged(const uint8_t* q8, const float* q_scale, const float* w,
                              const uint8_t* k8_cache, const float* k_scale_cache, int64_t n_pages,

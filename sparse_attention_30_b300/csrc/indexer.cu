@@ -274,10 +274,10 @@ cudaError_t launch_t(const CUtensorMap& qm, const CUtensorMap& km, int max_keys,
 
 int indexer_supported_heads(int H_I, bool paged) {
   // prefill tiles always have 256 (token, head) columns; a decode tile has one token's
-  // H_I columns and the epilogue drains them 64 at a time
+  // H_I columns and the epilogue drains them 32 at a time
   switch (H_I) {
-    case 4: case 8: case 16: case 32: return paged ? 0 : 1;
-    case 64: case 128: return 1;
+    case 4: case 8: case 16: return paged ? 0 : 1;
+    case 32: case 64: case 128: return 1;
     default: return 0;
   }
 }

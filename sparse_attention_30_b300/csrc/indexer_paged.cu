@@ -370,7 +370,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 }
 
-static_assert(PagedCfg<64>::SMEM <= 113 * 1024 && PagedCfg<128>::SMEM <= 113 * 1024, "two CTAs per SM");
+static_assert(PagedCfg<32>::SMEM <= 113 * 1024 && PagedCfg<64>::SMEM <= 113 * 1024 &&
+                  PagedCfg<128>::SMEM <= 113 * 1024,
+              "two CTAs per SM");
 
 template <int HI>
 cudaError_t launch_paged_t(const CUtensorMap& qm, const CUtensorMap& km, int max_keys, const IndexerArgs& a,
@@ -393,6 +395,7 @@ cudaError_t launch_paged_t(const CUtensorMap& qm, const CUtensorMap& km, int max
 cudaError_t launch_indexer_paged(const CUtensorMap& qm, const CUtensorMap& km, int H_I, int max_keys,
                                  const IndexerArgs& a, cudaStream_t stream) {
   switch (H_I) {
+    case 32: return launch_paged_t<32>(qm, km, max_keys, a, stream);
     case 64: return launch_paged_t<64>(qm, km, max_keys, a, stream);
     case 128: return launch_paged_t<128>(qm, km, max_keys, a, stream);
     default: return cudaErrorInvalidValue;

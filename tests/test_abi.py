@@ -84,7 +84,8 @@ def test_paged_index_rejects_unsupported_heads_and_pages():
     def call(H=64, page=64, bt_stride=2, max_len=128, ld=128, B=1):
         return f(A, A, A, A, A, 4, A, bt_stride, A, B, H, page, max_len, A, ld, None)
 
-    assert call(H=16) == 2              # decode tiles need H_I >= 64
+    assert call(H=16) == 2              # decode tiles need H_I of 32, 64 or 128
+    assert call(H=8) == 2
     assert call(page=48) == 1
     assert call(page=256) == 1
     assert call(bt_stride=1) == 1       # fewer table entries than max_len needs

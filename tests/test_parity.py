@@ -649,8 +649,9 @@ def test_forward_prefill_shape_sweep(dsa, L, H_I, H, k, chunk, q_pos0):
         _check_row(hinp, t, k, cfg.scale, idx[t], out[t], lse[t], q_pos0=q_pos0, where=f"sweep L={L} H={H} k={k}")
 
 
-_DECODE_SWEEP = [  # (B, H_I, H, k, page, ctx_lo, ctx_hi); the paged indexer takes H_I = 64 or 128
+_DECODE_SWEEP = [  # (B, H_I, H, k, page, ctx_lo, ctx_hi); the paged indexer takes H_I = 32, 64 or 128
     (1, 64, 1, 1, 16, 1, 1),            # one sequence of one token
+    (4, 32, 16, 64, 32, 50, 900),
     (3, 128, 5, 7, 16, 1, 200),
     (75, 64, 128, 64, 64, 64, 3000),    # more sequences than SM pairs: no key split
     (5, 128, 128, 2048, 64, 100, 5000),  # key split over few sequences, rows shorter than k
