@@ -232,3 +232,21 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, fn)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), fn
                 assert "oracle/" not in text, fn
+
+
+def test_decode_split_mirror_matches_library_workspace():
+    # the binding's decode_split mirrors the library's key-split choice; the library's decode
+    # workspace holds the fp32 partial outputs exactly when it splits, so the sizes must agree
+    dsa = _lib()
+    H, k, max_len = 128, 2048, 4096
+    for B in [1, 2, 5, 18, 19, 36, 37, 73, 74, 75, 200]:
+        d = dsa.ForwardArgs(mode=dsa.MODE_DECODE, H_I=64, H=H, k=k, scale=0.07, B=B, page_size=64,
+                            n_pages=B * 64, bt_stride=64, max_seq_len=max_len)
+        n = dsa.lib.dsa_forward_workspace_size(ctypes.byref(d))
+        r256 = lambda x: (x + 255) // 256 * 256
+        split = dsa.decode_split(B)
+        want = r256(B * max_len * 4) + r256(B * k * 4)
+        if split > 1:
+            want += r256(B * split * H * 512 * 4) + r256(B * split * H * 2 * 4)
+        assert n == want, (B, split, n, want)
+        assert split == (1 if B >= 74 else max(1, min(4, 74 // B)))
