@@ -250,3 +250,14 @@ def test_decode_split_mirror_matches_library_workspace():
             want += r256(B * split * H * 512 * 4) + r256(B * split * H * 2 * 4)
         assert n == want, (B, split, n, want)
         assert split == (1 if B >= 74 else max(1, min(4, 74 // B)))
+
+
+def test_default_prefill_chunk_keeps_the_score_block_near_one_gib():
+    # chunk_rows = 0 lets the library choose: about 1 GiB of fp32 scores, 256..8192 rows, at most T
+    dsa = _lib()
+    for S, T, want_chunk in [(131072, 131072, 2048), (4096, 4096, 4096), (65536, 100, 100), (1 << 22, 8192, 256)]:
+        a = dsa.ForwardArgs(mode=dsa.MODE_PREFILL, H_I=64, H=128, k=2048, scale=0.07, T=T, S=S, q_pos0=S - T,
+                            chunk_rows=0)
+        ld = (S + 3) // 4 * 4
+        r256 = lambda x: (x + 255) // 256 * 256
+        assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(a)) == r256(want_chunk * ld * 4) + r256(T * 2048 * 4)
