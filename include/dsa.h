@@ -78,7 +78,9 @@ int dsa_version(void);
  *   k8       [S, 128]       e4m3, 16-byte aligned
  *   k_scale  [S]            fp32 per-key scale
  *   scores   [T, ld]        fp32 output, ld >= min(S, q_pos0 + T), ld % 4 == 0, 16-byte aligned
- *   H_I must be a power of two in [1, 128]; T, S >= 1 (T = 0 is a no-op); q_pos0 >= 0.
+ *   H_I must be a power of two in [4, 128] (other powers of two up to 128 return
+ *   DSA_ERR_UNSUPPORTED, anything else DSA_ERR_INVALID_ARG); T, S >= 1 (T = 0 is a no-op);
+ *   q_pos0 >= 0.
  */
 dsa_status_t dsa_index(const uint8_t* q8, const float* q_scale, const float* w,
                        const uint8_t* k8, const float* k_scale,
@@ -240,7 +242,7 @@ enum { DSA_MODE_PREFILL = 0, DSA_MODE_DECODE = 1 };
  */
 typedef struct {
   int mode;           /* DSA_MODE_PREFILL or DSA_MODE_DECODE */
-  int H_I;            /* indexer heads (power of two, 1..128) */
+  int H_I;            /* indexer heads: prefill 4..128 (powers of two), decode 32, 64 or 128 */
   int H;              /* attention heads (1..128) */
   int k;              /* tokens selected per query (1..65536) */
   float scale;        /* softmax scale */

@@ -71,6 +71,8 @@ def test_index_rejects_bad_arguments_on_host():
     assert call(ld=4, T=8) == 1         # ld < min(S, pos + T)
     assert call(ld=4) == 4              # valid: with no GPU here it fails at the CUDA call
     assert call(H=48) == 1              # not a power of two
+    assert call(H=2) == 2               # powers of two below 4 are not built
+    assert call(H=1) == 2
     assert call(H=256) == 1
     assert call(S=0) == 1
     assert call(pos=-1) == 1
