@@ -359,8 +359,11 @@ dsa_status_t dsa_selftest_wait_timeout(int timeout_us, dsa_stream_t stream);
  *     make that first call before any stream capture.
  *   - Every call shares the array: calls whose work overlaps on the GPU race on it and
  *     must be ordered by the caller.  Nothing in it needs clearing between calls.
- *   - Otherwise identical to dsa_forward in decode mode (same kernels, same outputs);
- *     it allocates nothing and calls no allocating routine.
+ *   - Runs the same indexer, top-k and attention kernels as dsa_forward in decode mode, but
+ *     without the key split dsa_forward uses for fewer than 74 sequences (the split's partial
+ *     results would need more scratch): with few sequences it occupies fewer SMs and is slower,
+ *     and its outputs agree with dsa_forward's to rounding rather than bit for bit.  It
+ *     allocates nothing and calls no allocating routine.
  */
 dsa_status_t dsa_decode_noalloc(const dsa_forward_args* args, dsa_stream_t stream);
 
