@@ -387,3 +387,69 @@ def test_config1_golden_fixture():
         assert sorted(r["idx"].tolist()) == row["idx_sorted"]
         np.testing.assert_allclose(r["o"].sum(axis=1), row["o_rowsum"], rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(r["lse"], row["lse"], rtol=1e-12)
+
+
+# ---------------------------------------------------------------- the parity checker itself
+
+def test_attention_error_known_values_mixed_signs_over_rows_and_heads():
+    # Two tokens x three heads x four value dims.  The reference is far from zero and differs
+    # per element, so a relative error, a signed difference or a mean over the wrong axis gives
+    # a different pair of numbers than the one written out here.
+    ref = np.arange(24, dtype=np.float64).reshape(2, 3, 4) * 0.5 + 3.0
+    delta = np.zeros((2, 3, 4))
+    delta[0, 0, 0] = +0.25
+    delta[0, 2, 3] = -0.75    # the largest error is negative: a signed max would report +0.5
+    delta[1, 1, 2] = +0.5
+    delta[1, 2, 1] = -0.125
+    other = ref + delta
+    mx, mean = oracle.attention_error(ref, other)
+    assert mx == 0.75
+    assert mean == (0.25 + 0.75 + 0.5 + 0.125) / 24          # = 1.625 / 24 over all 24 entries
+    # symmetric in its arguments, zero on identical inputs, and bf16 output taken at its value
+    assert oracle.attention_error(other, ref) == (mx, mean)
+    assert oracle.attention_error(ref, ref) == (0.0, 0.0)
+    ob = torch.tensor(other).to(torch.bfloat16).double().numpy()
+    mx_b, _ = oracle.attention_error(ref, ob)
+    assert mx_b == np.abs(ref - ob).max()
+    # planted mistakes the checker must not make: each gives a different pair
+    assert (float(delta.max()), float(delta.mean())) != (mx, mean)                 # signed
+    assert float((np.abs(delta) / np.abs(ref)).max()) != mx                         # relative
+    assert float(np.abs(delta).mean(axis=-1).max()) != mean                         # wrong axis
+    assert oracle.attention_error(np.zeros((0, 4)), np.zeros((0, 4))) == (0.0, 0.0)
+
+
+def test_indexer_loss_sparse_path_scrambled_selection_against_torch_and_scipy():
+    """The sparse stage over a selection that is neither a prefix nor in order and holds -1 pads:
+    the target must come from the rows of those positions and the indexer distribution from the
+    scores at the same positions, slot by slot."""
+    from scipy.special import rel_entr, softmax
+    cfg = synth.config(1, k=16)
+    inp = synth.prefill_inputs(cfg)
+    t = 200
+    rng = np.random.default_rng(7)
+    keys = rng.permutation(t + 1)[:16]                       # 16 scrambled positions <= t
+    sel = np.full(24, -1, np.int64)
+    sel[: len(keys)] = keys                                  # padded like a selection row
+    got = oracle.indexer_loss_prefill_row(inp, t, cfg.k, cfg.scale, idx_override=sel)
+    assert got["keys"].tolist() == keys.tolist()
+    # target: torch's per-head softmax over the selected latent rows, averaged over heads
+    q = inp["q"][t].double()
+    c = inp["kv"][torch.as_tensor(keys)].double()
+    p_ref = torch.softmax(cfg.scale * (q @ c.T), dim=1).mean(dim=0).numpy()
+    np.testing.assert_allclose(got["p"], p_ref, rtol=1e-12, atol=1e-15)
+    # indexer scores at the same positions from torch's FP8 decode and a matmul
+    q8 = inp["q8"][t].view(torch.float8_e4m3fn).double()                       # [H_I, 128]
+    k8 = inp["k8"][torch.as_tensor(keys)].view(torch.float8_e4m3fn).double()   # [16, 128]
+    dots = (q8 @ k8.T) * inp["q_scale"][t].double()[:, None] * inp["k_scale"][torch.as_tensor(keys)].double()[None]
+    I_ref = (inp["w"][t].double()[:, None] * torch.relu(dots)).sum(0).numpy()
+    kl_ref = rel_entr(p_ref, softmax(I_ref)).sum()
+    assert abs(got["kl"] - kl_ref) <= 1e-12 * max(1.0, abs(kl_ref))
+    # a selection in another order gives the same KL with p permuted alongside
+    perm = rng.permutation(len(keys))
+    sel2 = np.concatenate([keys[perm], [-1] * 8])
+    got2 = oracle.indexer_loss_prefill_row(inp, t, cfg.k, cfg.scale, idx_override=sel2)
+    np.testing.assert_allclose(got2["p"], got["p"][perm], rtol=1e-13, atol=1e-16)
+    assert abs(got2["kl"] - got["kl"]) <= 1e-12 * max(1.0, abs(kl_ref))
+    # misaligned scores (the same positions' scores rolled by one slot) change the KL
+    I_bad = np.roll(I_ref, 1)
+    assert abs(rel_entr(p_ref, softmax(I_bad)).sum() - got["kl"]) > 1e-6
