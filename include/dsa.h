@@ -19,9 +19,19 @@
  *     finite fp32 (the score uses ReLU(sq*sk*x) = sq*sk*ReLU(x), which needs sq, sk > 0).
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream).  Argument
  *     errors are detected on the host and returned before anything is launched;
- *     a failed launch returns DSA_ERR_CUDA.  Device-side faults the kernels detect
- *     themselves (a wait that timed out, an index out of range) are recorded in a
- *     per-device status word that dsa_device_status() returns and clears.
+ *     a failed launch returns DSA_ERR_CUDA.
+ *   - Device-side faults the kernels detect themselves (a wait that timed out, an index
+ *     out of range) are recorded in a device status word (int32, 0 = DSA_OK; the first
+ *     error recorded stays until the word is cleared):
+ *       * calls that take a workspace (dsa_forward, dsa_forward_loss, dsa_prefill_host)
+ *         use the word at the start of their workspace; dsa_status(ws, stream) reads and
+ *         clears it.  That word must hold 0 before the workspace's first use (allocate it
+ *         zeroed, or clear its first 4 bytes);
+ *       * the per-stage calls take `dev_status`: a caller-owned device int32 (4-byte
+ *         aligned, zeroed before first use, read and cleared by dsa_status), or NULL for a
+ *         word shared by every call on the device (read and cleared by dsa_device_status).
+ *     So calls that may run at the same time on different streams or host threads each
+ *     report into their own word; only calls given NULL share one.
  *   - Every wait inside a kernel is bounded: after about one second it gives up, the
  *     kernel records DSA_ERR_DEVICE_TIMEOUT and returns.  The environment variable
  *     DSA_WAIT_LIMIT_MS (a positive integer, read once per process) sets another limit,
@@ -78,6 +88,7 @@ int dsa_version(void);
  *   k8       [S, 128]       e4m3, 16-byte aligned
  *   k_scale  [S]            fp32 per-key scale
  *   scores   [T, ld]        fp32 output, ld >= min(S, q_pos0 + T), ld % 4 == 0, 16-byte aligned
+ *   dev_status  device status word (see the conventions above), or NULL
  *   H_I must be a power of two in [4, 128] (other powers of two up to 128 return
  *   DSA_ERR_UNSUPPORTED, anything else DSA_ERR_INVALID_ARG); T, S >= 1 (T = 0 is a no-op);
  *   q_pos0 >= 0.
@@ -85,7 +96,7 @@ int dsa_version(void);
 dsa_status_t dsa_index(const uint8_t* q8, const float* q_scale, const float* w,
                        const uint8_t* k8, const float* k_scale,
                        int T, int S, int H_I, int64_t q_pos0,
-                       float* scores, int64_t ld, dsa_stream_t stream);
+                       float* scores, int64_t ld, int32_t* dev_status, dsa_stream_t stream);
 
 /*
  * dsa_index_paged — indexer scores of one new query token per sequence against a
@@ -103,12 +114,13 @@ dsa_status_t dsa_index(const uint8_t* q8, const float* q_scale, const float* w,
  *   page_size must divide 128 and be a multiple of 8; n_pages bounds the page numbers
  *   (an out-of-range page number is skipped and reported as DSA_ERR_DEVICE_RANGE).
  *   H_I must be 32, 64 or 128 (other head counts return DSA_ERR_UNSUPPORTED).
+ *   dev_status    device status word, or NULL
  */
 dsa_status_t dsa_index_paged(const uint8_t* q8, const float* q_scale, const float* w,
                              const uint8_t* k8_cache, const float* k_scale_cache, int64_t n_pages,
                              const int32_t* block_table, int64_t bt_stride,
                              const int32_t* seq_lens, int B, int H_I, int page_size, int max_seq_len,
-                             float* scores, int64_t ld, dsa_stream_t stream);
+                             float* scores, int64_t ld, int32_t* dev_status, dsa_stream_t stream);
 
 /*
  * dsa_topk — fine-grained token selection
@@ -149,11 +161,12 @@ dsa_status_t dsa_topk(const float* scores, int64_t ld, int T, const int32_t* row
  *       reported as DSA_ERR_DEVICE_RANGE)
  *   out [T, H, 512] bf16, 16-byte aligned
  *   lse [T, H] fp32 natural-log sum-exp of the scaled logits, or NULL
+ *   dev_status  device status word, or NULL
  */
 dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows,
                              const int32_t* block_table, int64_t bt_stride, int page_size,
                              const int32_t* idx, int T, int H, int k, float scale,
-                             uint16_t* out, float* lse, dsa_stream_t stream);
+                             uint16_t* out, float* lse, int32_t* dev_status, dsa_stream_t stream);
 
 /*
  * dsa_sparse_attn_split — dsa_sparse_attn with each row's selected keys spread over n_split
@@ -168,7 +181,7 @@ dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_
                                    const int32_t* block_table, int64_t bt_stride, int page_size,
                                    const int32_t* idx, int T, int H, int k, float scale,
                                    uint16_t* out, float* lse, int n_split, void* ws, size_t ws_bytes,
-                                   dsa_stream_t stream);
+                                   int32_t* dev_status, dsa_stream_t stream);
 
 /*
  * dsa_dense_causal_attn — dense causal attention in the same MQA mode of MLA: every row attends
@@ -188,12 +201,12 @@ dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_
  *   lse [T, H] fp32 natural-log sum-exp of the scaled logits, or NULL
  * Same arithmetic as dsa_sparse_attn (bf16 tensor-core products, fp32 accumulation and softmax);
  * the latent rows are read as contiguous 64-row tiles.  Errors: DSA_ERR_INVALID_ARG /
- * DSA_ERR_UNSUPPORTED before any launch; DSA_ERR_CUDA if the launch fails; device timeouts in the
- * status word (dsa_device_status).
+ * DSA_ERR_UNSUPPORTED before any launch; DSA_ERR_CUDA if the launch fails; device timeouts in
+ * `dev_status` (or, when it is NULL, the shared word read by dsa_device_status).
  */
 dsa_status_t dsa_dense_causal_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, int T, int H,
                                    int64_t q_pos0, float scale, uint16_t* out, float* lse,
-                                   dsa_stream_t stream);
+                                   int32_t* dev_status, dsa_stream_t stream);
 
 /*
  * dsa_indexer_loss — the lightning indexer's training objective
@@ -221,7 +234,7 @@ dsa_status_t dsa_dense_causal_attn(const uint16_t* q, const uint16_t* kv, int64_
 dsa_status_t dsa_indexer_loss(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* idx,
                               int T, int H, int k, int64_t q_pos0, float scale, const float* lse,
                               const float* scores, int64_t ld, float* p, float* kl, double* loss_acc,
-                              dsa_stream_t stream);
+                              int32_t* dev_status, dsa_stream_t stream);
 
 /* Forward modes. */
 enum { DSA_MODE_PREFILL = 0, DSA_MODE_DECODE = 1 };
@@ -273,14 +286,18 @@ typedef struct {
   int32_t* idx;
 } dsa_forward_args;
 
-/* Bytes of device workspace dsa_forward needs for these arguments (0 on invalid args). */
+/* Bytes of device workspace dsa_forward needs for these arguments (0 on invalid args): a 256-byte
+ * head whose first word is the call's status word, then the fp32 score block, the selection (when
+ * args->idx is NULL) and, for decode with fewer than 74 sequences, the key-split partial results. */
 size_t dsa_forward_workspace_size(const dsa_forward_args* args);
 
 /*
  * dsa_forward — the whole hot path: scores (dsa_index / dsa_index_paged), selection
  * (dsa_topk) and attention (dsa_sparse_attn), asynchronously on `stream`.
  * `ws` is a caller-owned device buffer of at least dsa_forward_workspace_size(args)
- * bytes, 256-byte aligned; it holds the fp32 score block and the selection.
+ * bytes, 256-byte aligned; its first word is the status word the kernels of this call report
+ * into (zero before the first use; dsa_status(ws, stream) reads and clears it), the rest holds
+ * the fp32 score block and the selection.
  */
 dsa_status_t dsa_forward(const dsa_forward_args* args, void* ws, size_t ws_bytes,
                          dsa_stream_t stream);
@@ -303,8 +320,9 @@ size_t dsa_forward_loss_workspace_size(const dsa_forward_args* args, int stage);
  *                          beyond validation).
  * Outputs: out, lse, idx (sparse stage, when non-NULL) as for dsa_forward; kl [T] per-row KL
  * terms (device, or NULL); *loss_acc (one device double, or NULL) has sum_t KL_t ADDED to it.
- * `ws`: dsa_forward_loss_workspace_size(args, stage) bytes, 256-byte aligned (the fp32 score
- * block of one chunk, and the selection when args->idx is NULL).  Errors as dsa_forward.
+ * `ws`: dsa_forward_loss_workspace_size(args, stage) bytes, 256-byte aligned (the status word
+ * head as in dsa_forward, the fp32 score block of one chunk, and the selection when args->idx is
+ * NULL).  Errors as dsa_forward.
  */
 dsa_status_t dsa_forward_loss(const dsa_forward_args* args, int stage, float* kl, double* loss_acc, void* ws,
                               size_t ws_bytes, dsa_stream_t stream);
@@ -319,7 +337,7 @@ dsa_status_t dsa_forward_loss(const dsa_forward_args* args, int stage, float* kl
  * asynchronous only from page-locked (pinned) host memory; pageable memory works but
  * serialises them.
  * `ws` is a caller-owned device buffer of at least dsa_prefill_host_workspace_size(args) bytes,
- * 256-byte aligned.  The call only enqueues work: the kernels run on `stream` and the copies on
+ * 256-byte aligned, starting with the status word head of dsa_forward.  The call only enqueues work: the kernels run on `stream` and the copies on
  * two streams the library keeps per device, ordered after the work already on `stream`; the
  * outputs are in host memory once `stream` reaches the point after this call (synchronise it
  * before reading them, and do not touch the host buffers before then).  Errors as dsa_forward;
@@ -330,19 +348,33 @@ dsa_status_t dsa_prefill_host(const dsa_forward_args* args, void* ws, size_t ws_
                               dsa_stream_t stream);
 
 /*
- * dsa_device_status — synchronises `stream`, then returns and clears the status word
- * the kernels write on the current device (DSA_OK if nothing was recorded).
- * Returns DSA_ERR_CUDA if the synchronisation itself fails.
+ * dsa_status — the device-side status of the calls that reported into `status_word`: a
+ * workspace of dsa_forward / dsa_forward_loss / dsa_prefill_host (its first word), or a
+ * caller-owned int32 passed as `dev_status` to the per-stage calls.  Reads the word after the
+ * work already enqueued on `stream` (the host waits for that work), returns it (DSA_OK if
+ * nothing was recorded) and clears it on the same stream, so that later work on `stream`
+ * records into a clean word.  DSA_ERR_INVALID_ARG for a NULL or misaligned pointer,
+ * DSA_ERR_CUDA if the copy or the synchronisation fails.  Calls on other streams that report
+ * into the same word must be ordered by the caller.
+ */
+dsa_status_t dsa_status(void* status_word, dsa_stream_t stream);
+
+/*
+ * dsa_device_status — dsa_status for the word shared by every call on the current device that
+ * was given no status word of its own (dev_status NULL, and dsa_decode_noalloc).  Every stream
+ * records into this one word, so with concurrent streams an error may be read by the wrong
+ * caller: give such calls their own words.
  */
 dsa_status_t dsa_device_status(dsa_stream_t stream);
 
 /*
  * dsa_selftest_wait_timeout — launches one block that waits on a barrier nobody
  * arrives at, with a limit of timeout_us microseconds; the kernel then records
- * DSA_ERR_DEVICE_TIMEOUT and returns.  Used to test the bounded-wait path without a
- * hang.  Follow with dsa_device_status().
+ * DSA_ERR_DEVICE_TIMEOUT into dev_status (or the shared word when NULL) and returns.
+ * Used to test the bounded-wait path without a hang.  Follow with dsa_status() /
+ * dsa_device_status().
  */
-dsa_status_t dsa_selftest_wait_timeout(int timeout_us, dsa_stream_t stream);
+dsa_status_t dsa_selftest_wait_timeout(int timeout_us, int32_t* dev_status, dsa_stream_t stream);
 
 /*
  * dsa_decode_noalloc — the decode forward (mode DSA_MODE_DECODE of dsa_forward) for callers
@@ -359,6 +391,8 @@ dsa_status_t dsa_selftest_wait_timeout(int timeout_us, dsa_stream_t stream);
  *     make that first call before any stream capture.
  *   - Every call shares the array: calls whose work overlaps on the GPU race on it and
  *     must be ordered by the caller.  Nothing in it needs clearing between calls.
+ *   - Every argument is checked before the first launch.  Device-side errors go to the
+ *     shared word of dsa_device_status (there is no workspace to hold a word of its own).
  *   - Runs the same indexer, top-k and attention kernels as dsa_forward in decode mode, but
  *     without the key split dsa_forward uses for fewer than 74 sequences (the split's partial
  *     results would need more scratch): with few sequences it occupies fewer SMs and is slower,

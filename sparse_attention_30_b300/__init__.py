@@ -26,7 +26,7 @@ EXPORTS = ("dsa_status_string", "dsa_version", "dsa_index", "dsa_index_paged", "
            "dsa_decode_noalloc", "dsa_decode_noalloc_capacity", "dsa_sparse_attn_split_workspace_size",
            "dsa_sparse_attn_split", "dsa_prefill_host_workspace_size", "dsa_prefill_host",
            "dsa_dense_causal_attn", "dsa_indexer_loss", "dsa_wait_limit_ns", "dsa_forward_loss_workspace_size",
-           "dsa_forward_loss")
+           "dsa_forward_loss", "dsa_status")
 
 
 class DSAError(RuntimeError):
@@ -63,21 +63,22 @@ def _load():
     sig = {
         "dsa_status_string": ([I], ctypes.c_char_p),
         "dsa_version": ([], I),
-        "dsa_index": ([P, P, P, P, P, I, I, I, I64, P, I64, P], I),
-        "dsa_index_paged": ([P, P, P, P, P, I64, P, I64, P, I, I, I, I, P, I64, P], I),
+        "dsa_index": ([P, P, P, P, P, I, I, I, I64, P, I64, P, P], I),
+        "dsa_index_paged": ([P, P, P, P, P, I64, P, I64, P, I, I, I, I, P, I64, P, P], I),
         "dsa_topk": ([P, I64, I, P, I64, I64, I, P, P], I),
-        "dsa_sparse_attn": ([P, P, I64, P, I64, I, P, I, I, I, F, P, P, P], I),
+        "dsa_sparse_attn": ([P, P, I64, P, I64, I, P, I, I, I, F, P, P, P, P], I),
         "dsa_forward_workspace_size": ([ctypes.POINTER(ForwardArgs)], ctypes.c_size_t),
         "dsa_forward": ([ctypes.POINTER(ForwardArgs), P, ctypes.c_size_t, P], I),
         "dsa_device_status": ([P], I),
-        "dsa_selftest_wait_timeout": ([I, P], I),
+        "dsa_status": ([P, P], I),
+        "dsa_selftest_wait_timeout": ([I, P, P], I),
         "dsa_decode_noalloc": ([ctypes.POINTER(ForwardArgs), P], I),
         "dsa_decode_noalloc_capacity": ([], ctypes.c_size_t),
         "dsa_sparse_attn_split_workspace_size": ([I, I, I], ctypes.c_size_t),
-        "dsa_dense_causal_attn": ([P, P, I64, I, I, I64, F, P, P, P], I),
+        "dsa_dense_causal_attn": ([P, P, I64, I, I, I64, F, P, P, P, P], I),
         "dsa_wait_limit_ns": ([], ctypes.c_uint64),
-        "dsa_indexer_loss": ([P, P, I64, P, I, I, I, I64, F, P, P, I64, P, P, P, P], I),
-        "dsa_sparse_attn_split": ([P, P, I64, P, I64, I, P, I, I, I, F, P, P, I, P, ctypes.c_size_t, P], I),
+        "dsa_indexer_loss": ([P, P, I64, P, I, I, I, I64, F, P, P, I64, P, P, P, P, P], I),
+        "dsa_sparse_attn_split": ([P, P, I64, P, I64, I, P, I, I, I, F, P, P, I, P, ctypes.c_size_t, P, P], I),
         "dsa_prefill_host_workspace_size": ([ctypes.POINTER(ForwardArgs)], ctypes.c_size_t),
         "dsa_forward_loss_workspace_size": ([ctypes.POINTER(ForwardArgs), I], ctypes.c_size_t),
         "dsa_forward_loss": ([ctypes.POINTER(ForwardArgs), I, P, P, P, ctypes.c_size_t, P], I),
@@ -114,12 +115,25 @@ def _need(t, dtype, name, dims=None):
 
 
 def device_status(stream=None) -> int:
-    """Synchronises the stream and returns (and clears) the device-side status word."""
+    """Status recorded in the device's shared word (calls given no status word of their own), read
+    after the stream's work and cleared (dsa_device_status)."""
     s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream()
     return lib.dsa_device_status(s)
 
 
-def index(q8, q_scale, w, k8, k_scale, q_pos0=0, scores=None):
+def status_word(device="cuda"):
+    """A zeroed device int32 status word for the per-stage calls' `status` argument."""
+    return torch.zeros((1,), dtype=torch.int32, device=device)
+
+
+def read_status(word, stream=None) -> int:
+    """Status recorded in `word` (a status_word() tensor or a workspace), read after the stream's work
+    and cleared on that stream (dsa_status)."""
+    s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(word)
+    return lib.dsa_status(_ptr(word), s)
+
+
+def index(q8, q_scale, w, k8, k_scale, q_pos0=0, scores=None, status=None):
     """Indexer scores of prefill rows (dsa_index). Returns scores [T, ld] fp32 (s <= pos written)."""
     _need(q8, torch.uint8, "q8", 3)
     _need(k8, torch.uint8, "k8", 2)
@@ -131,11 +145,12 @@ def index(q8, q_scale, w, k8, k_scale, q_pos0=0, scores=None):
     if scores is None:
         scores = torch.empty((T, ld), dtype=torch.float32, device=q8.device)
     _check(lib.dsa_index(_ptr(q8), _ptr(q_scale), _ptr(w), _ptr(k8), _ptr(k_scale), T, S, H_I, q_pos0,
-                         _ptr(scores), scores.stride(0), _stream(q8)), "dsa_index")
+                         _ptr(scores), scores.stride(0), _ptr(status), _stream(q8)), "dsa_index")
     return scores
 
 
-def index_paged(q8, q_scale, w, k8_cache, k_scale_cache, block_table, seq_lens, max_seq_len, scores=None):
+def index_paged(q8, q_scale, w, k8_cache, k_scale_cache, block_table, seq_lens, max_seq_len, scores=None,
+                status=None):
     """Decode indexer scores against a paged FP8 key cache (dsa_index_paged). Returns [B, ld] fp32."""
     _need(q8, torch.uint8, "q8", 3)
     _need(k8_cache, torch.uint8, "k8_cache", 3)
@@ -148,7 +163,7 @@ def index_paged(q8, q_scale, w, k8_cache, k_scale_cache, block_table, seq_lens, 
         scores = torch.empty((B, ld), dtype=torch.float32, device=q8.device)
     _check(lib.dsa_index_paged(_ptr(q8), _ptr(q_scale), _ptr(w), _ptr(k8_cache), _ptr(k_scale_cache), n_pages,
                                _ptr(block_table), block_table.stride(0), _ptr(seq_lens), B, H_I, page, max_seq_len,
-                               _ptr(scores), scores.stride(0), _stream(q8)), "dsa_index_paged")
+                               _ptr(scores), scores.stride(0), _ptr(status), _stream(q8)), "dsa_index_paged")
     return scores
 
 
@@ -164,7 +179,7 @@ def topk(scores, k, q_pos0=0, n_cols=None, row_lens=None, idx=None):
     return idx
 
 
-def sparse_attn(q, kv, idx, scale, block_table=None, page_size=0, out=None, lse=None, want_lse=True):
+def sparse_attn(q, kv, idx, scale, block_table=None, page_size=0, out=None, lse=None, want_lse=True, status=None):
     """Attention over the selected latent rows (dsa_sparse_attn). Returns (out [T,H,512] bf16, lse [T,H] | None).
 
     kv is [S, 576] (contiguous) or [n_pages, page_size, 576] with block_table [T, P].
@@ -184,11 +199,11 @@ def sparse_attn(q, kv, idx, scale, block_table=None, page_size=0, out=None, lse=
         lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
     bt_stride = block_table.stride(0) if block_table is not None else 0
     _check(lib.dsa_sparse_attn(_ptr(q), _ptr(kv), n_rows, _ptr(block_table), bt_stride, page_size, _ptr(idx), T, H,
-                               k, float(scale), _ptr(out), _ptr(lse), _stream(q)), "dsa_sparse_attn")
+                               k, float(scale), _ptr(out), _ptr(lse), _ptr(status), _stream(q)), "dsa_sparse_attn")
     return out, lse
 
 
-def dense_causal_attn(q, kv, scale, q_pos0=0, out=None, lse=None, want_lse=True):
+def dense_causal_attn(q, kv, scale, q_pos0=0, out=None, lse=None, want_lse=True, status=None):
     """Dense causal attention over every latent row up to each row's position (dsa_dense_causal_attn):
     the dense MLA baseline.  q [T, H, 576] holds rows at positions q_pos0 .. q_pos0 + T - 1, kv [S, 576].
     Returns (out [T,H,512] bf16, lse [T,H] | None)."""
@@ -200,11 +215,12 @@ def dense_causal_attn(q, kv, scale, q_pos0=0, out=None, lse=None, want_lse=True)
     if lse is None and want_lse:
         lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
     _check(lib.dsa_dense_causal_attn(_ptr(q), _ptr(kv), kv.shape[0], T, H, int(q_pos0), float(scale), _ptr(out),
-                                     _ptr(lse), _stream(q)), "dsa_dense_causal_attn")
+                                     _ptr(lse), _ptr(status), _stream(q)), "dsa_dense_causal_attn")
     return out, lse
 
 
-def indexer_loss(q, kv, lse, scores, scale, idx=None, q_pos0=0, p=None, kl=None, loss=None, want_p=True):
+def indexer_loss(q, kv, lse, scores, scale, idx=None, q_pos0=0, p=None, kl=None, loss=None, want_p=True,
+                 status=None):
     """The indexer's KL training loss (dsa_indexer_loss).  idx [T, k] selects the sparse stage (target
     over each row's selected set); idx=None is the dense warm-up over every position <= q_pos0 + t.
     lse [T, H] comes from the forward over the same sets, scores [T, ld] from the indexer.
@@ -226,7 +242,8 @@ def indexer_loss(q, kv, lse, scores, scale, idx=None, q_pos0=0, p=None, kl=None,
     if loss is None:
         loss = torch.zeros((1,), dtype=torch.float64, device=q.device)
     _check(lib.dsa_indexer_loss(_ptr(q), _ptr(kv), kv.shape[0], _ptr(idx), T, H, k, int(q_pos0), float(scale),
-                                _ptr(lse), _ptr(scores), scores.stride(0), _ptr(p), _ptr(kl), _ptr(loss), _stream(q)),
+                                _ptr(lse), _ptr(scores), scores.stride(0), _ptr(p), _ptr(kl), _ptr(loss), _ptr(status),
+                                _stream(q)),
            "dsa_indexer_loss")
     return p, kl, loss
 
@@ -236,7 +253,7 @@ def decode_split(B: int) -> int:
     return 1 if B <= 0 or B >= 74 else max(1, min(4, 74 // B))
 
 
-def sparse_attn_split(q, kv, idx, scale, n_split, block_table=None, out=None, lse=None, ws=None):
+def sparse_attn_split(q, kv, idx, scale, n_split, block_table=None, out=None, lse=None, ws=None, status=None):
     """dsa_sparse_attn_split: attention with each row's keys spread over n_split partial passes."""
     _need(q, torch.bfloat16, "q", 3)
     _need(kv, torch.bfloat16, "kv")
@@ -251,7 +268,8 @@ def sparse_attn_split(q, kv, idx, scale, n_split, block_table=None, out=None, ls
     bt_stride = block_table.stride(0) if block_table is not None else 0
     _check(lib.dsa_sparse_attn_split(_ptr(q), _ptr(kv), kv.numel() // 576, _ptr(block_table), bt_stride, page_size,
                                      _ptr(idx), T, H, idx.shape[1], float(scale), _ptr(out), _ptr(lse), n_split,
-                                     _ptr(ws), 0 if ws is None else ws.numel(), _stream(q)), "dsa_sparse_attn_split")
+                                     _ptr(ws), 0 if ws is None else ws.numel(), _ptr(status), _stream(q)),
+           "dsa_sparse_attn_split")
     return out, lse
 
 
@@ -269,7 +287,7 @@ class Forward:
         n = lib.dsa_forward_workspace_size(ctypes.byref(args))
         if n == 0:
             raise DSAError(1, "dsa_forward_workspace_size")
-        self.ws = torch.empty(n, dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(n, dtype=torch.uint8, device=device)  # the status word at its head starts at 0
 
     @classmethod
     def prefill(cls, inp, k, scale, q_pos0=0, chunk_rows=0, out=None, lse=None, idx=None):
@@ -308,6 +326,10 @@ class Forward:
         _check(lib.dsa_forward(ctypes.byref(self.args), _ptr(self.ws), self.ws.numel(), s), "dsa_forward")
         return self.out
 
+    def status(self, stream=None) -> int:
+        """Device-side status of the calls made with this workspace since the last read (dsa_status)."""
+        return read_status(self.ws, stream)
+
 
 LOSS_SPARSE, LOSS_DENSE_WARMUP = 0, 1
 
@@ -341,7 +363,7 @@ class ForwardLoss:
         n = lib.dsa_forward_loss_workspace_size(ctypes.byref(self.args), stage)
         if n == 0:
             raise DSAError(1, "dsa_forward_loss_workspace_size")
-        self.ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(n, dtype=torch.uint8, device=dev)
 
     def __call__(self, stream=None):
         s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(self.out)
@@ -349,6 +371,10 @@ class ForwardLoss:
         _check(lib.dsa_forward_loss(ctypes.byref(self.args), self.stage, _ptr(self.kl), _ptr(self.loss), _ptr(self.ws),
                                     self.ws.numel(), s), "dsa_forward_loss")
         return self.loss
+
+    def status(self, stream=None) -> int:
+        """Device-side status of the calls made with this workspace since the last read (dsa_status)."""
+        return read_status(self.ws, stream)
 
 
 class PrefillHost:
@@ -380,7 +406,7 @@ class PrefillHost:
         if n == 0:
             raise DSAError(1, "dsa_prefill_host_workspace_size")
         self.device = torch.device(device)
-        self.ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+        self.ws = torch.zeros(n, dtype=torch.uint8, device=self.device)
 
     def __call__(self, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
@@ -388,8 +414,13 @@ class PrefillHost:
                                     ctypes.c_void_p(s.cuda_stream)), "dsa_prefill_host")
         return self.out
 
+    def status(self, stream=None) -> int:
+        """Device-side status of the calls made with this workspace since the last read (dsa_status)."""
+        return read_status(self.ws, stream if stream is not None else torch.cuda.current_stream(self.device))
 
-def selftest_wait_timeout(timeout_us=2000):
-    """Runs the bounded-wait self-test kernel and returns the status it recorded (expects DSA_ERR_DEVICE_TIMEOUT)."""
-    _check(lib.dsa_selftest_wait_timeout(timeout_us, _stream()), "dsa_selftest_wait_timeout")
-    return device_status()
+
+def selftest_wait_timeout(timeout_us=2000, status=None):
+    """Runs the bounded-wait self-test kernel and returns the status it recorded (expects DSA_ERR_DEVICE_TIMEOUT)
+    in `status` (a status_word() tensor) or, when None, in the device's shared word."""
+    _check(lib.dsa_selftest_wait_timeout(timeout_us, _ptr(status), _stream()), "dsa_selftest_wait_timeout")
+    return device_status() if status is None else read_status(status)

@@ -103,9 +103,7 @@ cudaError_t launch_wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStr
 
 using namespace dsa;
 
-namespace {
-
-dsa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+namespace dsa {
 
 dsa_status_t check_index_args(const uint8_t* q8, const float* q_scale, const float* w, const uint8_t* k8,
                               const float* k_scale, int T, int S, int H_I, int64_t q_pos0, const float* scores,
@@ -157,7 +155,20 @@ dsa_status_t check_attn_args(const uint16_t* q, const uint16_t* kv, int64_t n_kv
   return DSA_OK;
 }
 
-// Workspace layout of dsa_forward: [scores block (fp32)] [selection (int32), if not caller-owned]
+int* status_target(int32_t* dev_status) { return dev_status ? dev_status : status_ptr(); }
+
+}  // namespace dsa
+
+namespace {
+
+dsa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+// Every workspace starts with a 256-byte head whose first word is the status word of the calls
+// that use it (read and cleared by dsa_status).
+constexpr size_t kStatusHead = 256;
+
+// Workspace layout of dsa_forward: [status head] [scores block (fp32)] [selection (int32), if not
+// caller-owned] [key-split partial results (decode with few sequences)]
 struct FwdPlan {
   int rows;          // query rows in total
   int chunk;         // rows scored per indexer / top-k launch
@@ -203,13 +214,13 @@ dsa_status_t plan_forward(const dsa_forward_args* a, FwdPlan* p) {
   p->part_o_bytes = p->n_split > 1 ? align256(static_cast<size_t>(p->rows) * p->n_split * a->H * 512 * 4) : 0;
   p->part_ml_bytes = p->n_split > 1 ? align256(static_cast<size_t>(p->rows) * p->n_split * a->H * 2 * 4) : 0;
   // (same layout as dsa_sparse_attn_split's workspace: partial outputs, then partial max / sum)
-  p->total = p->scores_bytes + p->idx_bytes + p->part_o_bytes + p->part_ml_bytes;
+  p->total = kStatusHead + p->scores_bytes + p->idx_bytes + p->part_o_bytes + p->part_ml_bytes;
   return DSA_OK;
 }
 
-// Device workspace of dsa_prefill_host: the keys once, then two slots of query-row chunk inputs
-// and outputs (so that the copies of one chunk overlap the kernels of the other), and one score
-// block.
+// Device workspace of dsa_prefill_host: the status head, the keys once, then two slots of query-row
+// chunk inputs and outputs (so that the copies of one chunk overlap the kernels of the other), and
+// one score block.
 struct HostPlan {
   FwdPlan f;
   size_t k8, k_scale, kv;                  // keys
@@ -234,7 +245,7 @@ dsa_status_t plan_prefill_host(const dsa_forward_args* a, HostPlan* h) {
   h->lse = align256(C * a->H * 4);
   h->slot = h->q8 + h->q_scale + h->w + h->q + h->idx + h->out + h->lse;
   h->scores = h->f.scores_bytes;
-  h->total = h->k8 + h->k_scale + h->kv + 2 * h->slot + h->scores;
+  h->total = kStatusHead + h->k8 + h->k_scale + h->kv + 2 * h->slot + h->scores;
   return DSA_OK;
 }
 
@@ -271,14 +282,14 @@ const char* dsa_status_string(dsa_status_t s) {
   return "DSA_ERR_UNKNOWN";
 }
 
-int dsa_version(void) { return (1 << 16) | 0; }
+int dsa_version(void) { return (2 << 16) | 0; }
 
 dsa_status_t dsa_index(const uint8_t* q8, const float* q_scale, const float* w, const uint8_t* k8,
                        const float* k_scale, int T, int S, int H_I, int64_t q_pos0, float* scores, int64_t ld,
-                       dsa_stream_t stream) {
+                       int32_t* dev_status, dsa_stream_t stream) {
   dsa_status_t st = check_index_args(q8, q_scale, w, k8, k_scale, T, S, H_I, q_pos0, scores, ld);
   if (st != DSA_OK || T == 0) return st;
-  int* status = status_ptr();
+  int* status = status_target(dev_status);
   if (!status) return DSA_ERR_CUDA;
   IndexerArgs a{};
   a.q_scale = q_scale; a.w = w; a.k_scale = k_scale;
@@ -291,11 +302,11 @@ dsa_status_t dsa_index(const uint8_t* q8, const float* q_scale, const float* w, 
 dsa_status_t dsa_index_paged(const uint8_t* q8, const float* q_scale, const float* w, const uint8_t* k8_cache,
                              const float* k_scale_cache, int64_t n_pages, const int32_t* block_table,
                              int64_t bt_stride, const int32_t* seq_lens, int B, int H_I, int page_size,
-                             int max_seq_len, float* scores, int64_t ld, dsa_stream_t stream) {
+                             int max_seq_len, float* scores, int64_t ld, int32_t* dev_status, dsa_stream_t stream) {
   dsa_status_t st = check_paged_index_args(q8, q_scale, w, k8_cache, k_scale_cache, n_pages, block_table, bt_stride,
                                            seq_lens, B, H_I, page_size, max_seq_len, scores, ld);
   if (st != DSA_OK || B == 0) return st;
-  int* status = status_ptr();
+  int* status = status_target(dev_status);
   if (!status) return DSA_ERR_CUDA;
   IndexerArgs a{};
   a.q_scale = q_scale; a.w = w; a.k_scale = k_scale_cache;
@@ -317,10 +328,10 @@ namespace {
 dsa_status_t sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* block_table,
                                int64_t bt_stride, int page_size, const int32_t* idx, int T, int H, int k, float scale,
                                uint16_t* out, float* lse, int n_split, float* part_o, float* part_ml,
-                               cudaStream_t stream) {
+                               int32_t* dev_status, cudaStream_t stream) {
   dsa_status_t st = check_attn_args(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, out);
   if (st != DSA_OK || T == 0) return st;
-  int* status = status_ptr();
+  int* status = status_target(dev_status);
   if (!status) return DSA_ERR_CUDA;
   AttnArgs a{};
   a.q = q; a.kv = kv; a.n_kv_rows = n_kv_rows; a.block_table = block_table; a.bt_stride = bt_stride;
@@ -349,11 +360,11 @@ extern "C" dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t*
                                               const int32_t* block_table, int64_t bt_stride, int page_size,
                                               const int32_t* idx, int T, int H, int k, float scale, uint16_t* out,
                                               float* lse, int n_split, void* ws, size_t ws_bytes,
-                                              dsa_stream_t stream) {
+                                              int32_t* dev_status, dsa_stream_t stream) {
   if (n_split < 1 || n_split > 8) return DSA_ERR_INVALID_ARG;
   if (n_split == 1)
     return sparse_attn_split(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, scale, out, lse, 1,
-                             nullptr, nullptr, stream);
+                             nullptr, nullptr, dev_status, stream);
   dsa_status_t st = check_attn_args(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, out);
   if (st != DSA_OK || T == 0) return st;
   const size_t need = dsa_sparse_attn_split_workspace_size(T, H, n_split);
@@ -361,26 +372,26 @@ extern "C" dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t*
   char* w = static_cast<char*>(ws);
   return sparse_attn_split(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, scale, out, lse, n_split,
                            reinterpret_cast<float*>(w), reinterpret_cast<float*>(w + split_part_o_bytes(T, H, n_split)),
-                           stream);
+                           dev_status, stream);
 }
 
 extern "C" dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows,
                                         const int32_t* block_table, int64_t bt_stride, int page_size,
                                         const int32_t* idx, int T, int H, int k, float scale, uint16_t* out,
-                                        float* lse, dsa_stream_t stream) {
+                                        float* lse, int32_t* dev_status, dsa_stream_t stream) {
   return sparse_attn_split(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, scale, out, lse, 1,
-                           nullptr, nullptr, stream);
+                           nullptr, nullptr, dev_status, stream);
 }
 
 extern "C" dsa_status_t dsa_dense_causal_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, int T, int H,
                                               int64_t q_pos0, float scale, uint16_t* out, float* lse,
-                                              dsa_stream_t stream) {
+                                              int32_t* dev_status, dsa_stream_t stream) {
   if (T < 0 || H < 1 || q_pos0 < 0 || n_kv_rows < 1 || n_kv_rows > INT32_MAX) return DSA_ERR_INVALID_ARG;
   if (q_pos0 + static_cast<int64_t>(T) > n_kv_rows) return DSA_ERR_INVALID_ARG;
   if (!q || !kv || !out || !aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
   if (H > 128) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
-  int* status = status_ptr();
+  int* status = status_target(dev_status);
   if (!status) return DSA_ERR_CUDA;
   AttnArgs a{};
   a.q = q; a.kv = kv; a.n_kv_rows = n_kv_rows; a.idx = nullptr; a.T = T; a.H = H; a.k = 0; a.q_pos0 = q_pos0;
@@ -392,7 +403,7 @@ extern "C" dsa_status_t dsa_dense_causal_attn(const uint16_t* q, const uint16_t*
 extern "C" dsa_status_t dsa_indexer_loss(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* idx,
                                          int T, int H, int k, int64_t q_pos0, float scale, const float* lse,
                                          const float* scores, int64_t ld, float* p, float* kl, double* loss_acc,
-                                         dsa_stream_t stream) {
+                                         int32_t* dev_status, dsa_stream_t stream) {
   if (T < 0 || H < 1 || n_kv_rows < 1 || n_kv_rows > INT32_MAX || ld < 1) return DSA_ERR_INVALID_ARG;
   if (!q || !kv || !lse || !scores || !aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
   if (idx) {
@@ -404,7 +415,7 @@ extern "C" dsa_status_t dsa_indexer_loss(const uint16_t* q, const uint16_t* kv, 
   }
   if (H > 128) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
-  int* status = status_ptr();
+  int* status = status_target(dev_status);
   if (!status) return DSA_ERR_CUDA;
   AttnArgs a{};
   a.q = q; a.kv = kv; a.n_kv_rows = n_kv_rows; a.idx = idx; a.T = T; a.H = H; a.k = idx ? k : 0;
@@ -429,8 +440,10 @@ dsa_status_t dsa_forward(const dsa_forward_args* a, void* ws, size_t ws_bytes, d
     return DSA_ERR_INVALID_ARG;
   if (p.rows == 0) return DSA_OK;
   if (!ws || ws_bytes < p.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
-  float* scores = static_cast<float*>(ws);
-  int32_t* idx = a->idx ? a->idx : reinterpret_cast<int32_t*>(static_cast<char*>(ws) + p.scores_bytes);
+  int32_t* wst = static_cast<int32_t*>(ws);
+  char* body = static_cast<char*>(ws) + kStatusHead;
+  float* scores = reinterpret_cast<float*>(body);
+  int32_t* idx = a->idx ? a->idx : reinterpret_cast<int32_t*>(body + p.scores_bytes);
   cudaStream_t s = stream;
 
   if (a->mode == DSA_MODE_PREFILL) {
@@ -443,27 +456,31 @@ dsa_status_t dsa_forward(const dsa_forward_args* a, void* ws, size_t ws_bytes, d
       const int64_t pos0 = a->q_pos0 + r0;
       st = dsa_index(a->q8 + static_cast<int64_t>(r0) * a->H_I * 128, a->q_scale + static_cast<int64_t>(r0) * a->H_I,
                      a->w + static_cast<int64_t>(r0) * a->H_I, a->k8, a->k_scale, rows, a->S, a->H_I, pos0, scores,
-                     p.ld, s);
+                     p.ld, wst, s);
       if (st != DSA_OK) return st;
       st = dsa_topk(scores, p.ld, rows, nullptr, a->S, pos0, a->k, idx + static_cast<int64_t>(r0) * a->k, s);
       if (st != DSA_OK) return st;
     }
-    return dsa_sparse_attn(a->q, a->kv, a->S, nullptr, 0, 0, idx, a->T, a->H, a->k, a->scale, a->out, a->lse, s);
+    return dsa_sparse_attn(a->q, a->kv, a->S, nullptr, 0, 0, idx, a->T, a->H, a->k, a->scale, a->out, a->lse, wst,
+                           s);
   }
   // decode
   st = check_paged_index_args(a->q8, a->q_scale, a->w, a->k8, a->k_scale, a->n_pages, a->block_table, a->bt_stride,
                               a->seq_lens, a->B, a->H_I, a->page_size, a->max_seq_len, scores, p.ld);
   if (st != DSA_OK) return st;
+  st = check_attn_args(a->q, a->kv, a->n_pages * a->page_size, a->block_table, a->bt_stride, a->page_size, idx, a->B,
+                       a->H, a->k, a->out);
+  if (st != DSA_OK) return st;
   st = dsa_index_paged(a->q8, a->q_scale, a->w, a->k8, a->k_scale, a->n_pages, a->block_table, a->bt_stride,
-                       a->seq_lens, a->B, a->H_I, a->page_size, a->max_seq_len, scores, p.ld, s);
+                       a->seq_lens, a->B, a->H_I, a->page_size, a->max_seq_len, scores, p.ld, wst, s);
   if (st != DSA_OK) return st;
   st = dsa_topk(scores, p.ld, a->B, a->seq_lens, p.ld, 0, a->k, idx, s);
   if (st != DSA_OK) return st;
-  char* part = static_cast<char*>(ws) + p.scores_bytes + p.idx_bytes;
+  char* part = body + p.scores_bytes + p.idx_bytes;
   return sparse_attn_split(a->q, a->kv, a->n_pages * a->page_size, a->block_table, a->bt_stride, a->page_size, idx,
                            a->B, a->H, a->k, a->scale, a->out, a->lse, p.n_split,
                            p.n_split > 1 ? reinterpret_cast<float*>(part) : nullptr,
-                           p.n_split > 1 ? reinterpret_cast<float*>(part + p.part_o_bytes) : nullptr, s);
+                           p.n_split > 1 ? reinterpret_cast<float*>(part + p.part_o_bytes) : nullptr, wst, s);
 }
 
 size_t dsa_forward_loss_workspace_size(const dsa_forward_args* args, int stage) {
@@ -471,7 +488,7 @@ size_t dsa_forward_loss_workspace_size(const dsa_forward_args* args, int stage) 
   if (!args || args->mode != DSA_MODE_PREFILL || (stage != DSA_LOSS_SPARSE && stage != DSA_LOSS_DENSE_WARMUP) ||
       plan_forward(args, &p) != DSA_OK)
     return 0;
-  return stage == DSA_LOSS_SPARSE ? p.total : p.scores_bytes;
+  return stage == DSA_LOSS_SPARSE ? p.total : kStatusHead + p.scores_bytes;
 }
 
 dsa_status_t dsa_forward_loss(const dsa_forward_args* a, int stage, float* kl, double* loss_acc, void* ws,
@@ -485,11 +502,12 @@ dsa_status_t dsa_forward_loss(const dsa_forward_args* a, int stage, float* kl, d
     return DSA_ERR_INVALID_ARG;
   if (p.rows == 0) return DSA_OK;
   const bool sparse = stage == DSA_LOSS_SPARSE;
-  const size_t need = sparse ? p.total : p.scores_bytes;
+  const size_t need = sparse ? p.total : kStatusHead + p.scores_bytes;
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
-  float* scores = static_cast<float*>(ws);
-  int32_t* idx = !sparse ? nullptr
-                         : a->idx ? a->idx : reinterpret_cast<int32_t*>(static_cast<char*>(ws) + p.scores_bytes);
+  int32_t* wst = static_cast<int32_t*>(ws);
+  char* body = static_cast<char*>(ws) + kStatusHead;
+  float* scores = reinterpret_cast<float*>(body);
+  int32_t* idx = !sparse ? nullptr : a->idx ? a->idx : reinterpret_cast<int32_t*>(body + p.scores_bytes);
   st = check_index_args(a->q8, a->q_scale, a->w, a->k8, a->k_scale, a->T, a->S, a->H_I, a->q_pos0, scores, p.ld);
   if (st != DSA_OK) return st;
   if (sparse) {
@@ -506,21 +524,21 @@ dsa_status_t dsa_forward_loss(const dsa_forward_args* a, int stage, float* kl, d
     float* kl_c = kl ? kl + r0 : nullptr;
     st = dsa_index(a->q8 + static_cast<int64_t>(r0) * a->H_I * 128, a->q_scale + static_cast<int64_t>(r0) * a->H_I,
                    a->w + static_cast<int64_t>(r0) * a->H_I, a->k8, a->k_scale, rows, a->S, a->H_I, pos0, scores,
-                   p.ld, s);
+                   p.ld, wst, s);
     if (st != DSA_OK) return st;
     if (sparse) {
       int32_t* idx_c = idx + static_cast<int64_t>(r0) * a->k;
       st = dsa_topk(scores, p.ld, rows, nullptr, a->S, pos0, a->k, idx_c, s);
       if (st != DSA_OK) return st;
-      st = dsa_sparse_attn(q, a->kv, a->S, nullptr, 0, 0, idx_c, rows, a->H, a->k, a->scale, out, lse, s);
+      st = dsa_sparse_attn(q, a->kv, a->S, nullptr, 0, 0, idx_c, rows, a->H, a->k, a->scale, out, lse, wst, s);
       if (st != DSA_OK) return st;
       st = dsa_indexer_loss(q, a->kv, a->S, idx_c, rows, a->H, a->k, 0, a->scale, lse, scores, p.ld, nullptr, kl_c,
-                            loss_acc, s);
+                            loss_acc, wst, s);
     } else {
-      st = dsa_dense_causal_attn(q, a->kv, a->S, rows, a->H, pos0, a->scale, out, lse, s);
+      st = dsa_dense_causal_attn(q, a->kv, a->S, rows, a->H, pos0, a->scale, out, lse, wst, s);
       if (st != DSA_OK) return st;
       st = dsa_indexer_loss(q, a->kv, a->S, nullptr, rows, a->H, 0, pos0, a->scale, lse, scores, p.ld, nullptr, kl_c,
-                            loss_acc, s);
+                            loss_acc, wst, s);
     }
     if (st != DSA_OK) return st;
   }
@@ -542,7 +560,8 @@ dsa_status_t dsa_prefill_host(const dsa_forward_args* a, void* ws, size_t ws_byt
   if (a->T == 0) return DSA_OK;
   if (!ws || ws_bytes < hp.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
   const int C = hp.f.chunk, H_I = a->H_I, H = a->H, K = a->k;
-  char* p = static_cast<char*>(ws);
+  int32_t* wst = static_cast<int32_t*>(ws);
+  char* p = static_cast<char*>(ws) + kStatusHead;
   uint8_t* k8 = reinterpret_cast<uint8_t*>(p);
   float* k_scale = reinterpret_cast<float*>(p + hp.k8);
   uint16_t* kv = reinterpret_cast<uint16_t*>(p + hp.k8 + hp.k_scale);
@@ -603,9 +622,10 @@ dsa_status_t dsa_prefill_host(const dsa_forward_args* a, void* ws, size_t ws_byt
          (c < 2 || cudaStreamWaitEvent(s, out_done[b], 0) == cudaSuccess);
     if (!ok) break;
     const int64_t pos0 = a->q_pos0 + r0;
-    st = dsa_index(q.q8, q.q_scale, q.w, k8, k_scale, rows, a->S, H_I, pos0, scores, hp.f.ld, s);
+    st = dsa_index(q.q8, q.q_scale, q.w, k8, k_scale, rows, a->S, H_I, pos0, scores, hp.f.ld, wst, s);
     if (st == DSA_OK) st = dsa_topk(scores, hp.f.ld, rows, nullptr, a->S, pos0, K, q.idx, s);
-    if (st == DSA_OK) st = dsa_sparse_attn(q.q, kv, a->S, nullptr, 0, 0, q.idx, rows, H, K, a->scale, q.out, q.lse, s);
+    if (st == DSA_OK)
+      st = dsa_sparse_attn(q.q, kv, a->S, nullptr, 0, 0, q.idx, rows, H, K, a->scale, q.out, q.lse, wst, s);
     if (st != DSA_OK) break;
     ok = cudaEventRecord(comp_done[b], s) == cudaSuccess;
     // outputs of chunk c back to the host
@@ -627,20 +647,30 @@ dsa_status_t dsa_prefill_host(const dsa_forward_args* a, void* ws, size_t ws_byt
   return ok ? DSA_OK : DSA_ERR_CUDA;
 }
 
-dsa_status_t dsa_device_status(dsa_stream_t stream) {
+// Reads a device status word after the work already on `stream`, and clears it on the same stream
+// (so that no later work of that stream can record into it between the read and the clear).
+static dsa_status_t read_and_clear(int32_t* word, cudaStream_t stream) {
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return DSA_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
-  int* p = status_ptr();
-  if (!p) return DSA_ERR_CUDA;
-  int v = 0;
-  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
-  const int zero = 0;
-  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return DSA_ERR_CUDA;
+  if (v != 0 && cudaMemsetAsync(word, 0, sizeof(v), stream) != cudaSuccess) return DSA_ERR_CUDA;
   return static_cast<dsa_status_t>(v);
 }
 
-dsa_status_t dsa_selftest_wait_timeout(int timeout_us, dsa_stream_t stream) {
-  if (timeout_us < 1 || timeout_us > 10000000) return DSA_ERR_INVALID_ARG;
+dsa_status_t dsa_status(void* status_word, dsa_stream_t stream) {
+  if (!status_word || (reinterpret_cast<uintptr_t>(status_word) & 3u)) return DSA_ERR_INVALID_ARG;
+  return read_and_clear(static_cast<int32_t*>(status_word), stream);
+}
+
+dsa_status_t dsa_device_status(dsa_stream_t stream) {
   int* p = status_ptr();
+  if (!p) return DSA_ERR_CUDA;
+  return read_and_clear(p, stream);
+}
+
+dsa_status_t dsa_selftest_wait_timeout(int timeout_us, int32_t* dev_status, dsa_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 10000000) return DSA_ERR_INVALID_ARG;
+  int* p = status_target(dev_status);
   if (!p) return DSA_ERR_CUDA;
   return from_cuda(launch_wait_timeout_selftest(p, static_cast<uint64_t>(timeout_us) * 1000ull, stream));
 }

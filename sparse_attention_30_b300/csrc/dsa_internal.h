@@ -99,6 +99,24 @@ struct AttnArgs {
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- host-side argument checks (api.cu)
+
+// Each returns DSA_OK, or the status the public call returns before launching anything.
+dsa_status_t check_index_args(const uint8_t* q8, const float* q_scale, const float* w, const uint8_t* k8,
+                              const float* k_scale, int T, int S, int H_I, int64_t q_pos0, const float* scores,
+                              int64_t ld);
+dsa_status_t check_paged_index_args(const uint8_t* q8, const float* q_scale, const float* w, const uint8_t* k8c,
+                                    const float* ksc, int64_t n_pages, const int32_t* bt, int64_t bt_stride,
+                                    const int32_t* lens, int B, int H_I, int page, int max_len, const float* scores,
+                                    int64_t ld);
+dsa_status_t check_topk_args(const float* scores, int64_t ld, int T, int64_t n_cols, int64_t q_pos0, int k,
+                             const int32_t* idx, const int32_t* row_lens);
+dsa_status_t check_attn_args(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* bt,
+                             int64_t bt_stride, int page, const int32_t* idx, int T, int H, int k,
+                             const uint16_t* out);
+// The device word a call reports into: the caller's (non-NULL) or this device's shared word.
+int* status_target(int32_t* dev_status);
+
 // ---------------------------------------------------------------- self test
 
 cudaError_t launch_wait_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);

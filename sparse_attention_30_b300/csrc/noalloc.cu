@@ -50,6 +50,25 @@ extern "C" dsa_status_t dsa_decode_noalloc(const dsa_forward_args* a, dsa_stream
   const size_t idx_bytes = a->idx ? 0 : round256(static_cast<size_t>(a->B) * a->k * sizeof(int32_t));
   if (score_bytes + idx_bytes > kNoAllocBytes) return DSA_ERR_WORKSPACE;
 
+  // Every argument of the three stages is checked before anything else, so that a rejected call
+  // leaves the caller's buffers (idx included) untouched.  The checks of the scratch pointers look
+  // only at null and alignment; the array is non-null and 256-byte aligned, which the stand-in
+  // address below shares.
+  {
+    float* scores_standin = reinterpret_cast<float*>(static_cast<uintptr_t>(256));
+    int32_t* idx_standin = a->idx ? a->idx : reinterpret_cast<int32_t*>(static_cast<uintptr_t>(256));
+    if (!a->q || !a->kv || !a->out) return DSA_ERR_INVALID_ARG;
+    dsa_status_t st = check_paged_index_args(a->q8, a->q_scale, a->w, a->k8, a->k_scale, a->n_pages, a->block_table,
+                                             a->bt_stride, a->seq_lens, a->B, a->H_I, a->page_size, a->max_seq_len,
+                                             scores_standin, ld);
+    if (st != DSA_OK) return st;
+    st = check_topk_args(scores_standin, ld, a->B, ld, 0, a->k, idx_standin, a->seq_lens);
+    if (st != DSA_OK) return st;
+    st = check_attn_args(a->q, a->kv, a->n_pages * a->page_size, a->block_table, a->bt_stride, a->page_size,
+                         idx_standin, a->B, a->H, a->k, a->out);
+    if (st != DSA_OK) return st;
+  }
+
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
   void* base = nullptr;
@@ -65,12 +84,13 @@ extern "C" dsa_status_t dsa_decode_noalloc(const dsa_forward_args* a, dsa_stream
   float* scores = static_cast<float*>(base);
   int32_t* idx = a->idx ? a->idx : reinterpret_cast<int32_t*>(static_cast<char*>(base) + score_bytes);
 
+  // the kernels report into the per-device status word (dsa_device_status)
   dsa_status_t st = dsa_index_paged(a->q8, a->q_scale, a->w, a->k8, a->k_scale, a->n_pages, a->block_table,
                                     a->bt_stride, a->seq_lens, a->B, a->H_I, a->page_size, a->max_seq_len, scores,
-                                    ld, stream);
+                                    ld, nullptr, stream);
   if (st != DSA_OK) return st;
   st = dsa_topk(scores, ld, a->B, a->seq_lens, ld, 0, a->k, idx, stream);
   if (st != DSA_OK) return st;
   return dsa_sparse_attn(a->q, a->kv, a->n_pages * a->page_size, a->block_table, a->bt_stride, a->page_size, idx,
-                         a->B, a->H, a->k, a->scale, a->out, a->lse, stream);
+                         a->B, a->H, a->k, a->scale, a->out, a->lse, nullptr, stream);
 }

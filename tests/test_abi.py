@@ -48,7 +48,7 @@ def test_status_strings_and_version():
     for code, name in dsa.STATUS_NAMES.items():
         assert dsa.lib.dsa_status_string(code).decode() == name
     assert dsa.lib.dsa_status_string(99).decode() == "DSA_ERR_UNKNOWN"
-    assert dsa.lib.dsa_version() >> 16 == 1
+    assert dsa.lib.dsa_version() >> 16 == 2
 
 
 # Fake, 16-byte-aligned "device" addresses: validation must reject the call before any of
@@ -63,7 +63,8 @@ def test_index_rejects_bad_arguments_on_host():
 
     def call(**kw):
         a = {**ok, **kw}
-        return f(a["q8"], a["qs"], a["w"], a["k8"], a["ks"], a["T"], a["S"], a["H"], a["pos"], a["sc"], a["ld"], None)
+        return f(a["q8"], a["qs"], a["w"], a["k8"], a["ks"], a["T"], a["S"], a["H"], a["pos"], a["sc"], a["ld"], None,
+                 None)
 
     assert call(q8=None) == 1
     assert call(k8=A + 8) == 1          # misaligned
@@ -84,7 +85,7 @@ def test_paged_index_rejects_unsupported_heads_and_pages():
     f = dsa.lib.dsa_index_paged
 
     def call(H=64, page=64, bt_stride=2, max_len=128, ld=128, B=1):
-        return f(A, A, A, A, A, 4, A, bt_stride, A, B, H, page, max_len, A, ld, None)
+        return f(A, A, A, A, A, 4, A, bt_stride, A, B, H, page, max_len, A, ld, None, None)
 
     assert call(H=16) == 2              # decode tiles need H_I of 32, 64 or 128
     assert call(H=8) == 2
@@ -104,29 +105,29 @@ def test_topk_and_attention_reject_bad_arguments_on_host():
     assert t(None, 8, 2, None, 8, 0, 4, A, None) == 1
     assert t(A, 8, 0, None, 8, 0, 4, A, None) == 0
     s = dsa.lib.dsa_sparse_attn
-    assert s(A, A, 10, None, 0, 0, A, 2, 129, 4, 0.1, A, None, None) == 2   # H > 128
-    assert s(A, A + 2, 10, None, 0, 0, A, 2, 8, 4, 0.1, A, None, None) == 1
-    assert s(A, A, 0, None, 0, 0, A, 2, 8, 4, 0.1, A, None, None) == 1
-    assert s(A, A, 10, None, 0, 0, A, 0, 8, 4, 0.1, A, None, None) == 0
+    assert s(A, A, 10, None, 0, 0, A, 2, 129, 4, 0.1, A, None, None, None) == 2   # H > 128
+    assert s(A, A + 2, 10, None, 0, 0, A, 2, 8, 4, 0.1, A, None, None, None) == 1
+    assert s(A, A, 0, None, 0, 0, A, 2, 8, 4, 0.1, A, None, None, None) == 1
+    assert s(A, A, 10, None, 0, 0, A, 0, 8, 4, 0.1, A, None, None, None) == 0
     d = dsa.lib.dsa_dense_causal_attn
-    assert d(A, A, 10, 2, 129, 0, 0.1, A, None, None) == 2          # H > 128
-    assert d(A, A, 10, 4, 8, 7, 0.1, A, None, None) == 1            # q_pos0 + T > n_kv_rows
-    assert d(A, A, 10, 2, 8, -1, 0.1, A, None, None) == 1           # negative position
-    assert d(A, A + 2, 10, 2, 8, 0, 0.1, A, None, None) == 1        # misaligned kv
-    assert d(None, A, 10, 2, 8, 0, 0.1, A, None, None) == 1
-    assert d(A, A, 1 << 31, 2, 8, 0, 0.1, A, None, None) == 1       # rows past int32
-    assert d(A, A, 10, 0, 8, 3, 0.1, A, None, None) == 0            # nothing to do
+    assert d(A, A, 10, 2, 129, 0, 0.1, A, None, None, None) == 2          # H > 128
+    assert d(A, A, 10, 4, 8, 7, 0.1, A, None, None, None) == 1            # q_pos0 + T > n_kv_rows
+    assert d(A, A, 10, 2, 8, -1, 0.1, A, None, None, None) == 1           # negative position
+    assert d(A, A + 2, 10, 2, 8, 0, 0.1, A, None, None, None) == 1        # misaligned kv
+    assert d(None, A, 10, 2, 8, 0, 0.1, A, None, None, None) == 1
+    assert d(A, A, 1 << 31, 2, 8, 0, 0.1, A, None, None, None) == 1       # rows past int32
+    assert d(A, A, 10, 0, 8, 3, 0.1, A, None, None, None) == 0            # nothing to do
     L = dsa.lib.dsa_indexer_loss
-    #        q  kv  n   idx   T  H  k  pos0 scale lse scores ld  p     kl    loss  stream
-    assert L(A, A, 10, A, 2, 129, 4, 0, 0.1, A, A, 16, None, None, None, None) == 2     # H > 128
-    assert L(A, A, 10, A, 2, 8, 0, 0, 0.1, A, A, 16, None, None, None, None) == 1       # k = 0
-    assert L(A, A, 10, A, 2, 8, 4, 0, 0.1, None, A, 16, None, None, None, None) == 1    # no lse
-    assert L(A, A, 10, A, 2, 8, 4, 0, 0.1, A, None, 16, None, None, None, None) == 1    # no scores
-    assert L(A, A, 10, None, 4, 8, 0, 7, 0.1, A, A, 16, None, None, None, None) == 1    # dense: rows past keys
-    assert L(A, A, 20, None, 4, 8, 0, 7, 0.1, A, A, 10, None, None, None, None) == 1    # dense: rows past ld
-    assert L(A, A, 20, None, 4, 8, 0, 0, 0.1, A, A, 10, A, None, None, None) == 1       # dense: no per-slot target
-    assert L(A, A + 2, 10, A, 2, 8, 4, 0, 0.1, A, A, 16, None, None, None, None) == 1   # misaligned kv
-    assert L(A, A, 10, A, 0, 8, 4, 0, 0.1, A, A, 16, None, None, None, None) == 0       # nothing to do
+    #        q  kv  n   idx   T  H  k  pos0 scale lse scores ld  p     kl    loss  status stream
+    assert L(A, A, 10, A, 2, 129, 4, 0, 0.1, A, A, 16, None, None, None, None, None) == 2     # H > 128
+    assert L(A, A, 10, A, 2, 8, 0, 0, 0.1, A, A, 16, None, None, None, None, None) == 1       # k = 0
+    assert L(A, A, 10, A, 2, 8, 4, 0, 0.1, None, A, 16, None, None, None, None, None) == 1    # no lse
+    assert L(A, A, 10, A, 2, 8, 4, 0, 0.1, A, None, 16, None, None, None, None, None) == 1    # no scores
+    assert L(A, A, 10, None, 4, 8, 0, 7, 0.1, A, A, 16, None, None, None, None, None) == 1    # dense: rows past keys
+    assert L(A, A, 20, None, 4, 8, 0, 7, 0.1, A, A, 10, None, None, None, None, None) == 1    # dense: rows past ld
+    assert L(A, A, 20, None, 4, 8, 0, 0, 0.1, A, A, 10, A, None, None, None, None) == 1  # dense: no per-slot target
+    assert L(A, A + 2, 10, A, 2, 8, 4, 0, 0.1, A, A, 16, None, None, None, None, None) == 1   # misaligned kv
+    assert L(A, A, 10, A, 0, 8, 4, 0, 0.1, A, A, 16, None, None, None, None, None) == 0       # nothing to do
 
 
 def test_wait_limit_default_and_environment_override():
@@ -152,13 +153,13 @@ def test_forward_workspace_and_validation():
     a = dsa.ForwardArgs(mode=dsa.MODE_PREFILL, H_I=64, H=128, k=2048, scale=0.07, T=4096, S=4096, q_pos0=0,
                         chunk_rows=1024)
     n = dsa.lib.dsa_forward_workspace_size(ctypes.byref(a))
-    # one 1024-row fp32 score block plus the int32 selection of all rows
-    assert n == 1024 * 4096 * 4 + 4096 * 2048 * 4
+    # the 256-byte status head, one 1024-row fp32 score block and the int32 selection of all rows
+    assert n == 256 + 1024 * 4096 * 4 + 4096 * 2048 * 4
     a.T = 5000                                        # q_pos0 + T > S
     assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(a)) == 0
     d = dsa.ForwardArgs(mode=dsa.MODE_DECODE, H_I=64, H=128, k=2048, scale=0.07, B=64, page_size=64,
                         n_pages=32768, bt_stride=512, max_seq_len=32768)
-    assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(d)) == 64 * 32768 * 4 + 64 * 2048 * 4
+    assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(d)) == 256 + 64 * 32768 * 4 + 64 * 2048 * 4
     d.mode = 7
     assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(d)) == 0
     d.mode = dsa.MODE_DECODE
@@ -171,10 +172,10 @@ def test_forward_loss_workspace_and_validation():
     a = dsa.ForwardArgs(mode=dsa.MODE_PREFILL, H_I=64, H=128, k=2048, scale=0.07, T=4096, S=4096, q_pos0=0,
                         chunk_rows=1024)
     ws = dsa.lib.dsa_forward_loss_workspace_size
-    # sparse stage: the score block of one chunk plus the selection of all rows (as dsa_forward)
-    assert ws(ctypes.byref(a), dsa.LOSS_SPARSE) == 1024 * 4096 * 4 + 4096 * 2048 * 4
-    # dense warm-up: the score block only
-    assert ws(ctypes.byref(a), dsa.LOSS_DENSE_WARMUP) == 1024 * 4096 * 4
+    # sparse stage: the status head, the score block of one chunk and the selection of all rows
+    assert ws(ctypes.byref(a), dsa.LOSS_SPARSE) == 256 + 1024 * 4096 * 4 + 4096 * 2048 * 4
+    # dense warm-up: the status head and the score block
+    assert ws(ctypes.byref(a), dsa.LOSS_DENSE_WARMUP) == 256 + 1024 * 4096 * 4
     assert ws(ctypes.byref(a), 2) == 0                                   # no such stage
     d = dsa.ForwardArgs(mode=dsa.MODE_DECODE, H_I=64, H=128, k=2048, scale=0.07, B=64, page_size=64,
                         n_pages=32768, bt_stride=512, max_seq_len=32768)
@@ -193,7 +194,7 @@ def test_prefill_host_workspace_and_validation():
     n = dsa.lib.dsa_prefill_host_workspace_size(ctypes.byref(a))
     keys = 4096 * 128 + 4096 * 4 + 4096 * 576 * 2
     slot = 1024 * (64 * 128 + 64 * 4 + 64 * 4 + 128 * 576 * 2 + 2048 * 4 + 128 * 512 * 2 + 128 * 4)
-    assert n == keys + 2 * slot + 1024 * 4096 * 4
+    assert n == 256 + keys + 2 * slot + 1024 * 4096 * 4
     a.mode = dsa.MODE_DECODE                          # prefill only
     assert dsa.lib.dsa_prefill_host_workspace_size(ctypes.byref(a)) == 0
     assert dsa.lib.dsa_prefill_host(ctypes.byref(a), None, 0, None) == 1
@@ -247,7 +248,7 @@ def test_decode_split_mirror_matches_library_workspace():
         n = dsa.lib.dsa_forward_workspace_size(ctypes.byref(d))
         r256 = lambda x: (x + 255) // 256 * 256
         split = dsa.decode_split(B)
-        want = r256(B * max_len * 4) + r256(B * k * 4)
+        want = 256 + r256(B * max_len * 4) + r256(B * k * 4)
         if split > 1:
             want += r256(B * split * H * 512 * 4) + r256(B * split * H * 2 * 4)
         assert n == want, (B, split, n, want)
@@ -262,4 +263,25 @@ def test_default_prefill_chunk_keeps_the_score_block_near_one_gib():
                             chunk_rows=0)
         ld = (S + 3) // 4 * 4
         r256 = lambda x: (x + 255) // 256 * 256
-        assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(a)) == r256(want_chunk * ld * 4) + r256(T * 2048 * 4)
+        assert dsa.lib.dsa_forward_workspace_size(ctypes.byref(a)) == 256 + r256(want_chunk * ld * 4) + r256(T * 2048 * 4)
+
+
+def test_status_reads_reject_bad_words_on_host():
+    dsa = _lib()
+    assert dsa.lib.dsa_status(None, None) == 1                # no word
+    assert dsa.lib.dsa_status(A + 2, None) == 1               # misaligned word
+    assert dsa.lib.dsa_selftest_wait_timeout(0, None, None) == 1
+
+
+def test_noalloc_decode_checks_every_argument_before_launching():
+    # a bad attention argument (misaligned output) is refused before the indexer and top-k are
+    # queued, so nothing touches the caller's buffers
+    dsa = _lib()
+    a = dsa.ForwardArgs(mode=dsa.MODE_DECODE, H_I=64, H=128, k=2048, scale=0.07, B=4, page_size=64, n_pages=64,
+                        bt_stride=16, max_seq_len=1024, block_table=A, seq_lens=A, q8=A, q_scale=A, w=A, k8=A,
+                        k_scale=A, q=A, kv=A, out=A + 8, idx=A)
+    assert dsa.lib.dsa_decode_noalloc(ctypes.byref(a), None) == 1
+    a.out, a.H = A, 200                                       # too many heads: unsupported
+    assert dsa.lib.dsa_decode_noalloc(ctypes.byref(a), None) == 2
+    a.H, a.kv = 128, None
+    assert dsa.lib.dsa_decode_noalloc(ctypes.byref(a), None) == 1

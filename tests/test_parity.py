@@ -428,7 +428,7 @@ def test_forward_loss_matches_the_separate_calls(dsa, stage):
     f = dsa.ForwardLoss(d, cfg.k, cfg.scale, stage=stage, chunk_rows=1024,
                         idx=torch.empty((cfg.L, cfg.k), dtype=torch.int32, device="cuda") if stage == 0 else None)
     loss = f().item()
-    assert dsa.device_status() == 0
+    assert f.status() == 0 and dsa.device_status() == 0
     kl_ref = torch.empty(cfg.L, device="cuda")
     ld = cfg.L
     scores = torch.empty((1024, ld), dtype=torch.float32, device="cuda")
@@ -482,7 +482,7 @@ def _run_prefill(dsa, d, cfg, chunk_rows=0):
     lse = torch.empty((cfg.L, cfg.H), dtype=torch.float32, device="cuda")
     f = dsa.Forward.prefill(d, cfg.k, cfg.scale, chunk_rows=chunk_rows, lse=lse, idx=idx)
     f()
-    assert dsa.device_status() == 0
+    assert f.status() == 0 and dsa.device_status() == 0
     return f
 
 
@@ -519,7 +519,7 @@ def test_prefill_host_matches_device_forward(dsa):
     for _ in range(2):  # twice: the second call reuses the slots and events
         g()
         torch.cuda.synchronize()
-        assert dsa.device_status() == 0
+        assert g.status() == 0 and dsa.device_status() == 0
         assert torch.equal(torch.sort(idx, dim=1).values, torch.sort(f.idx.cpu(), dim=1).values)
         diff = (g.out.float() - f.out.float().cpu()).abs()
         assert diff.max().item() <= MAX_TOL and diff.mean().item() <= 1e-4  # a bf16 ulp where the order differs
@@ -535,7 +535,7 @@ def test_forward_decode_full_config(dsa, cid):
     lse = torch.empty((cfg.B, cfg.H), dtype=torch.float32, device="cuda")
     f = dsa.Forward.decode(d, cfg.k, cfg.scale, max_len, lse=lse, idx=idx)
     f()
-    assert dsa.device_status() == 0
+    assert f.status() == 0 and dsa.device_status() == 0
     hinp = _host(d)
     idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
     for b in range(cfg.B):
@@ -551,7 +551,7 @@ def test_forward_decode_small_batch_splits_keys(dsa):
     lse = torch.empty((cfg.B, cfg.H), dtype=torch.float32, device="cuda")
     f = dsa.Forward.decode(d, cfg.k, cfg.scale, max_len, lse=lse, idx=idx)
     f()
-    assert dsa.device_status() == 0
+    assert f.status() == 0 and dsa.device_status() == 0
     hinp = _host(d)
     idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
     for b in range(cfg.B):
@@ -565,7 +565,7 @@ def test_forward_prefill_config4_full_size_sampled_rows(dsa):
     f = dsa.Forward.prefill(d, cfg.k, cfg.scale, lse=torch.empty((cfg.L, cfg.H), device="cuda"),
                             idx=torch.empty((cfg.L, cfg.k), dtype=torch.int32, device="cuda"))
     f()
-    assert dsa.device_status() == 0
+    assert f.status() == 0 and dsa.device_status() == 0
     rows = [0, 1, 2047, 2048, 5000, 65535, 65536, 100003, 131070, 131071]
     keys = {n: d[n].cpu() for n in ("k8", "k_scale", "kv")}
     for t in rows:
@@ -641,7 +641,7 @@ def test_forward_prefill_shape_sweep(dsa, L, H_I, H, k, chunk, q_pos0):
     lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
     f = dsa.Forward.prefill(d, k, cfg.scale, q_pos0=q_pos0, chunk_rows=chunk, lse=lse, idx=idx)
     f()
-    assert dsa.device_status() == 0
+    assert f.status() == 0 and dsa.device_status() == 0
     idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
     check = range(T) if T * H <= 8192 else sorted({0, 1, T // 3, T // 2, T - 2, T - 1})
     for t in check:
@@ -669,7 +669,7 @@ def test_forward_decode_shape_sweep(dsa, B, H_I, H, k, page, lo, hi):
     lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
     f = dsa.Forward.decode(d, k, cfg.scale, max_len, lse=lse, idx=idx)
     f()
-    assert dsa.device_status() == 0
+    assert f.status() == 0 and dsa.device_status() == 0
     idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
     for b in sorted({0, B // 2, B - 1}):
         _check_row(hinp, b, k, cfg.scale, idx[b], out[b], lse[b], decode=True, where=f"decode sweep B={B} H={H} k={k}")
@@ -678,10 +678,53 @@ def test_forward_decode_shape_sweep(dsa, B, H_I, H, k, page, lo, hi):
 # ----------------------------------------------------------------------------- failure path
 
 
+def test_status_words_are_per_call_on_two_streams(dsa):
+    """Calls on two streams, each with its own status word: the range error of one (an index past
+    the end of the latent rows, or a page number past the cache) is reported by that call only,
+    and neither reaches the device's shared word."""
+    g = torch.Generator().manual_seed(41)
+    S, T, k = 300, 6, 64
+    q = torch.randn(T, 8, 576, generator=g).to(torch.bfloat16).cuda()
+    kv = torch.randn(S, 576, generator=g).to(torch.bfloat16).cuda()
+    idx = torch.stack([torch.randperm(S, generator=g)[:k] for _ in range(T)]).to(torch.int32).cuda()
+    bad = idx.clone()
+    bad[2, 7] = S + 11
+    wa, wb = dsa.status_word(), dsa.status_word()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        with torch.cuda.stream(sa):
+            dsa.sparse_attn(q, kv, bad, 0.07, status=wa)
+        with torch.cuda.stream(sb):
+            dsa.sparse_attn(q, kv, idx, 0.07, status=wb)
+    assert dsa.read_status(wa, sa) == 6
+    assert dsa.read_status(wb, sb) == 0
+    assert dsa.device_status() == 0
+    assert dsa.read_status(wa, sa) == 0              # cleared by the read
+    # the fused decode forward: each call reports into the head of its own workspace
+    cfg = synth.config(3, B=4, ctx=2000, k=256, H=16, H_I=64)
+    d = _cuda(synth.decode_inputs(cfg))
+    d_bad = dict(d, block_table=d["block_table"].clone())
+    d_bad["block_table"][1, 3] = d["k8_cache"].shape[0] + 5          # a page past the cache
+    fa = dsa.Forward.decode(d_bad, cfg.k, cfg.scale, cfg.ctx)
+    fb = dsa.Forward.decode(d, cfg.k, cfg.scale, cfg.ctx)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        fa(sa)
+        fb(sb)
+    assert fa.status(sa) == 6
+    assert fb.status(sb) == 0
+    assert dsa.device_status() == 0
+    fa(sa)
+    assert fa.status(sa) == 6 and fa.status(sa) == 0
+
+
 def test_bounded_wait_times_out_and_context_survives(dsa):
     assert dsa.device_status() == 0
     assert dsa.selftest_wait_timeout(2000) == 5     # DSA_ERR_DEVICE_TIMEOUT, recorded and returned
     assert dsa.device_status() == 0                 # cleared
+    w = dsa.status_word()
+    assert dsa.selftest_wait_timeout(2000, status=w) == 5 and dsa.device_status() == 0
     x = torch.randn(2, 4096, device="cuda")
     idx = dsa.topk(x, 16)
     assert dsa.device_status() == 0 and idx.shape == (2, 16)

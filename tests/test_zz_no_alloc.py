@@ -29,20 +29,28 @@ def test_noalloc_decode_matches_forward_on_consecutive_calls(dsa):
         d = synth.decode_inputs(cfg, device="cuda")
         max_len = int(d["seq_lens"].max())
         lse_ref = torch.empty((cfg.B, cfg.H), dtype=torch.float32, device="cuda")
-        ref = dsa.Forward.decode(d, cfg.k, cfg.scale, max_len, lse=lse_ref)
+        idx_ref = torch.empty((cfg.B, cfg.k), dtype=torch.int32, device="cuda")
+        ref = dsa.Forward.decode(d, cfg.k, cfg.scale, max_len, lse=lse_ref, idx=idx_ref)
         ref()
-        assert dsa.device_status() == 0
-        out = torch.full_like(ref.out, float("nan"))
-        lse = torch.full_like(lse_ref, float("nan"))
-        args = dsa.ForwardArgs.from_buffer_copy(ref.args)
-        args.out, args.lse, args.idx = out.data_ptr(), lse.data_ptr(), None   # selection in the static scratch
-        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-        assert dsa.lib.dsa_decode_noalloc(ctypes.byref(args), stream) == 0
-        assert dsa.device_status() == 0
-        d_out = (out.float() - ref.out.float()).abs()
-        assert d_out.max().item() <= 2e-2 and d_out.mean().item() <= 2e-3, f"call {n}"
-        assert (lse - lse_ref).abs().max().item() <= 2e-3, f"call {n}"
-        assert not torch.isnan(out).any()
+        assert ref.status() == 0 and dsa.device_status() == 0
+        # the selection either stays in the static scratch (idx NULL) or goes to a caller-owned buffer,
+        # in which case the scratch holds only the scores
+        for own_idx in (False, True):
+            out = torch.full_like(ref.out, float("nan"))
+            lse = torch.full_like(lse_ref, float("nan"))
+            idx = torch.full_like(idx_ref, -7) if own_idx else None
+            args = dsa.ForwardArgs.from_buffer_copy(ref.args)
+            args.out, args.lse, args.idx = out.data_ptr(), lse.data_ptr(), idx.data_ptr() if own_idx else None
+            stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            assert dsa.lib.dsa_decode_noalloc(ctypes.byref(args), stream) == 0
+            assert dsa.device_status() == 0
+            where = f"call {n}, caller idx {own_idx}"
+            d_out = (out.float() - ref.out.float()).abs()
+            assert d_out.max().item() <= 2e-2 and d_out.mean().item() <= 2e-3, where
+            assert (lse - lse_ref).abs().max().item() <= 2e-3, where
+            assert not torch.isnan(out).any(), where
+            if own_idx:   # the same selected sets as dsa_forward's (slot order is not fixed)
+                assert torch.equal(torch.sort(idx, dim=1).values, torch.sort(idx_ref, dim=1).values), where
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(dsa):
