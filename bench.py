@@ -6,10 +6,11 @@ Default run (N=1): one step = the whole forward of one 128K-token prefill sequen
 `value` is prefill tokens/s; the decode figure (query tokens/s, B=32 mixed contexts up to
 128K) rides along under "decode".  Prints ONE JSON line on rank 0.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--shard sequences|rows]
 
 Under torchrun each rank runs its own 128K sequence (weak scaling, no collective on the
-data path); the step time is the max over ranks.
+data path); the step time is the max over ranks.  With --shard rows the ranks instead split
+one 128K sequence by query rows (strong scaling) and all-gather the keys every step.
 """
 from __future__ import annotations
 
@@ -42,6 +43,76 @@ def _peaks():
         return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p["bf16_tflops_sustained"],
                     src="measured")
     return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
+
+
+def measure_fp8_peak(n=8192, sustain_s=2.0):
+    """Dense FP8 e4m3 tensor throughput of this GPU, measured with torch._scaled_mm (cuBLASLt) on an
+    n x n x n product with bf16 output: the best of 10 timed launches (burst, for kernels timed alone)
+    and the mean over back-to-back launches for `sustain_s` seconds (sustained, for kernels timed
+    inside a long step).  Returns dict(burst, sustained) in TFLOP/s, or None if FP8 GEMMs are not
+    available."""
+    try:
+        g = torch.Generator(device="cuda").manual_seed(0)
+        a = torch.randn((n, n), device="cuda", generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device="cuda", generator=g).to(torch.float8_e4m3fn).t()  # column-major
+        one = torch.ones((), device="cuda")
+
+        def mm():
+            return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+        for _ in range(3):
+            mm()
+        torch.cuda.synchronize()
+        flop = 2.0 * n ** 3
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = _rec(), None
+            mm()
+            e1 = _rec()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        # sustained: as many launches as fill sustain_s at the burst rate, timed as one block
+        reps = max(10, int(sustain_s * 1e3 / best))
+        e0 = _rec()
+        for _ in range(reps):
+            mm()
+        e1 = _rec()
+        e1.synchronize()
+        sus = e0.elapsed_time(e1) / reps
+        del a, b
+        return {"burst": flop / (best * 1e-3) / 1e12, "sustained": flop / (sus * 1e-3) / 1e12,
+                "how": f"torch._scaled_mm e4m3 x e4m3 -> bf16, {n}^3, best of 10 / mean of {reps} back to back"}
+    except (RuntimeError, AttributeError, TypeError) as e:  # pragma: no cover (no FP8 GEMM on this build)
+        return {"error": str(e)[:200]}
+
+
+# DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of one kernel per unit of its work,
+# from a capture of a given build of that kernel's source.  A figure is reported only while the
+# source still hashes to the captured build; otherwise `traffic` is null.
+TRAFFIC_CAPTURES = {}
+
+
+def _src_hash(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "sparse_attention_30_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {"sparse_attn": ["sparse_attn.cu", "dsa_ptx.cuh"], "indexer": ["indexer.cu", "dsa_ptx.cuh"],
+                  "topk": ["topk.cu"]}
+
+
+def traffic_for(kernel, units):
+    """Captured DRAM bytes per unit x units, with the capture it comes from, or (None, reason)."""
+    cap = TRAFFIC_CAPTURES.get(kernel)
+    if cap is None:
+        return None, "no capture of this kernel"
+    if cap["src"] != _src_hash(KERNEL_SOURCES[kernel]):
+        return None, "kernel source changed since the capture"
+    return round(cap["bytes_per_unit"] * units), cap["capture"]
 
 
 class ClockSampler:
@@ -225,67 +296,86 @@ def run_ours(args, dist, rank, ws):
         return bench_dense_curve(dsa, synth, args, peaks)
     if args.workload == "indexer_loss":
         return bench_indexer_loss(dsa, synth, args, peaks)
+    if args.shard == "rows":
+        return bench_prefill_rows(dsa, synth, args, peaks, dist, rank, ws)
     cid = {"prefill128k": 4, "prefill4k": 2}[args.workload]
     cfg = synth.config(cid)
     if rank:
         cfg = synth.config(cid, seed=rank_seed(cfg.seed, rank))
     d = synth.prefill_inputs(cfg, device="cuda")
-    runner = PrefillRunner(dsa, d, cfg, args.chunk)
+    fp8 = measure_fp8_peak() if not args.no_fp8_peak else {"error": "not measured (--no-fp8-peak)"}
+    # the step the job is charged: dsa_forward (the library's fused entry point) over the sequence
+    idx = torch.empty((cfg.L, cfg.k), dtype=torch.int32, device="cuda")
+    lse = torch.empty((cfg.L, cfg.H), dtype=torch.float32, device="cuda")
+    fwd = dsa.Forward.prefill(d, cfg.k, cfg.scale, chunk_rows=args.chunk, lse=lse, idx=idx)
+    n_chunks = (cfg.L + args.chunk - 1) // args.chunk
 
     for _ in range(args.warmup):
-        runner.step()
-    st = dsa.device_status()
+        fwd()
+    st = fwd.status()
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
 
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    ev = {"index": [], "topk": [], "attn": []}
     _barrier(dist)
     t0, t1 = _rec(), None
     for _ in range(args.steps):
-        runner.step(ev)
+        fwd()
     t1 = _rec()
     _barrier(dist)
     clk = clocks.stop() if clocks else None
     total_ms = _max_over_ranks(dist, t0.elapsed_time(t1))
-    st = dsa.device_status()
+    st = fwd.status()
     if st != 0:
         raise RuntimeError(f"device status {st} in the timed region")
     ms_step = total_ms / args.steps
     value = aggregate_tokens_per_s(cfg.L, ws, args.steps, total_ms)
 
-    # per-kernel rooflines (algorithmic work / summed launch time over the timed region)
+    # per-kernel times: the same launches (same chunking, same stream), one binding call per launch
+    # with CUDA events around each, for as many steps again
+    runner = PrefillRunner(dsa, d, cfg, args.chunk)
+    ev = {"index": [], "topk": [], "attn": []}
+    runner.step()
+    _barrier(dist)
+    b0 = _rec()
+    for _ in range(args.steps):
+        runner.step(ev)
+    b1 = _rec()
+    _barrier(dist)
+    st = dsa.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the breakdown pass")
+    breakdown_ms = b0.elapsed_time(b1) / args.steps
+
+    # per-kernel rooflines (algorithmic work / summed launch time)
     w = prefill_work(cfg.L, cfg.H_I, cfg.H, cfg.k)
     t_index = _pairs_ms(ev["index"]) / args.steps
     t_topk = _pairs_ms(ev["topk"]) / args.steps
     t_attn = _pairs_ms(ev["attn"]) / args.steps
-    fp8_peak = 2.0 * peaks["bf16_sus"]
+    if "sustained" in fp8:
+        fp8_peak, fp8_src = fp8["sustained"], "measured e4m3 _scaled_mm (sustained)"
+    else:
+        fp8_peak, fp8_src = 2.0 * peaks["bf16_sus"], f"2 x {peaks['src']} bf16 sustained (FP8 not measured)"
     bf16_peak = peaks["bf16_sus"]
     kern = {
         "indexer": dict(bound="tensor", achieved=w["indexer_flop"] / (t_index * 1e-3) / 1e12, peak=fp8_peak,
-                        unit="TFLOP/s", ms=t_index, launches=runner.n_chunks),
+                        unit="TFLOP/s", ms=t_index, launches=n_chunks, peak_source=fp8_src,
+                        frac_of_2x_bf16_sustained=None),
         "topk": dict(bound="hbm", achieved=w["topk_bytes"] / (t_topk * 1e-3) / 1e9, peak=peaks["hbm"],
-                     unit="GB/s", ms=t_topk, launches=runner.n_chunks),
+                     unit="GB/s", ms=t_topk, launches=n_chunks, peak_source=f"{peaks['src']} copy bandwidth"),
         "sparse_attn": dict(bound="tensor", achieved=w["attn_flop"] / (t_attn * 1e-3) / 1e12, peak=bf16_peak,
-                            unit="TFLOP/s", ms=t_attn, launches=1),
+                            unit="TFLOP/s", ms=t_attn, launches=1, peak_source=f"{peaks['src']} bf16 sustained"),
     }
     for v in kern.values():
         v["frac"] = v["achieved"] / v["peak"]
+    kern["indexer"]["frac_of_2x_bf16_sustained"] = kern["indexer"]["achieved"] / (2.0 * peaks["bf16_sus"])
     dom_name = max(kern, key=lambda n: kern[n]["ms"])
     dom = kern[dom_name]
-    # DRAM bytes (read + write) per query row from the ncu capture of the 1024-row 128K tail
-    # (profiles/prefill128k_tail_full.md), scaled to the launch's rows; the capture starts from a
-    # flushed L2, so it overstates the steady state a little.  None where no capture matches.
-    traffic_per_row = {"sparse_attn": (0.496003e9 + 0.116915e9) / 1024, "indexer": (0.06382e9 + 0.475909e9) / 1024,
-                       "topk": (0.617335e9 + 0.007506e9) / 1024}
-    traffic = traffic_per_row.get(dom_name)
-    if traffic is not None:
-        traffic = round(traffic * cfg.L / kern[dom_name]["launches"])
+    # DRAM traffic per launch: the captured bytes per query row x the rows one launch covers
+    traffic, traffic_src = traffic_for(dom_name, cfg.L / kern[dom_name]["launches"])
     roofline = {"kernel": dom_name, "bound": dom["bound"], "achieved": round(dom["achieved"], 2),
-                "peak": dom["peak"], "unit": dom["unit"], "frac": round(dom["frac"], 4), "traffic": traffic,
-                "traffic_unit": "bytes per launch (ncu dram read + write, scaled from the 128K tail capture)",
-                "peak_source": f"{peaks['src']} (sustained; FP8 = 2 x bf16)" if dom["unit"] == "TFLOP/s"
-                else f"{peaks['src']} copy bandwidth"}
+                "peak": round(dom["peak"], 1), "unit": dom["unit"], "frac": round(dom["frac"], 4),
+                "traffic": traffic, "traffic_source": traffic_src, "peak_source": dom["peak_source"]}
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
@@ -298,7 +388,11 @@ def run_ours(args, dist, rank, ws):
             "roofline": roofline,
             "kernels": {n: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         for n, v in kern.items()},
-            "gpu_launches": runner.launches * args.steps,
+            "kernel_times": f"a second pass of {args.steps} steps making the same launches one binding call at a "
+                            f"time with CUDA events around each ({breakdown_ms:.3f} ms per step there)",
+            "fp8_peak_tflops": {k: (round(v, 1) if isinstance(v, float) else v) for k, v in fp8.items()},
+            "path": "dsa_forward (C ABI) via Forward.prefill, inputs resident in HBM",
+            "gpu_launches": (2 * n_chunks + 1) * args.steps,
             "clocks": clk}
 
     if not args.no_decode:
@@ -306,11 +400,74 @@ def run_ours(args, dist, rank, ws):
         line["decode_b64_32k"] = bench_decode(dsa, synth, args, peaks, cid=3)
     if not args.no_e2e:
         line["e2e"] = bench_e2e(dsa, d, cfg, args, dist, ws)
-    del d, runner
+    del d, runner, fwd
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_seconds)
     return line
+
+
+def bench_prefill_rows(dsa, synth, args, peaks, dist, rank, ws):
+    """One 128K prefill split by query rows over the ranks (strong scaling: the total work is one
+    sequence whatever N is).  Rank r owns the contiguous rows partition_rows gives it (balanced by
+    modelled time) and the keys of those positions; each step all-gathers every rank's indexer keys,
+    key scales and latent rows into local HBM (NCCL), then runs dsa_forward on its own rows with
+    q_pos0 at their first position.  The step time is the slowest rank's."""
+    from sparse_attention_30_b300 import shard
+    cfg = synth.config(4)
+    ranges = shard.partition_rows(cfg.L, ws, cfg.H_I, cfg.H, cfg.k, align=128)
+    r0, r1 = ranges[rank]
+    d = synth.prefill_inputs(cfg, device="cuda")     # the same sequence on every rank (same seed)
+    key_names = ("k8", "k_scale", "kv")
+    local_keys = {n: d[n][r0:r1].clone() for n in key_names}        # what this rank produced
+    keys = {n: torch.zeros_like(d[n]) for n in key_names}            # every position, filled each step
+    inp = {n: d[n][r0:r1].clone() for n in ("q8", "q_scale", "w", "q")}
+    inp.update(keys)
+    del d
+    torch.cuda.empty_cache()
+    T = r1 - r0
+    lse = torch.empty((T, cfg.H), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, cfg.k), dtype=torch.int32, device="cuda")
+    fwd = dsa.Forward.prefill(inp, cfg.k, cfg.scale, q_pos0=r0, chunk_rows=args.chunk, lse=lse, idx=idx)
+
+    def step():
+        for n in key_names:
+            if dist is None:
+                keys[n].copy_(local_keys[n])
+            else:
+                shard.all_gather_rows(local_keys[n], ranges, rank, out=keys[n])
+        if T > 0:
+            fwd()
+
+    for _ in range(args.warmup):
+        step()
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    _barrier(dist)
+    t0 = _rec()
+    for _ in range(args.steps):
+        step()
+    t1 = _rec()
+    _barrier(dist)
+    clk = clocks.stop() if clocks else None
+    my_ms = t0.elapsed_time(t1)
+    total_ms = _max_over_ranks(dist, my_ms)
+    st = fwd.status() if T > 0 else 0
+    if _max_over_ranks(dist, float(st)) != 0:
+        raise RuntimeError(f"device status {st} on rank {rank}")
+    value = cfg.L * args.steps / (total_ms / 1e3)
+    n_chunks = (T + args.chunk - 1) // args.chunk
+    return {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "fp8-e4m3 indexer / bf16 attention (fp32 accum)",
+            "data": "synthetic (seeded; shapes and distributions of the 128K prefill workload)",
+            "config": {"workload": f"one prefill L={cfg.L}, H_I=64, d_I=128, k=2048, H=128, D=576/512, query rows "
+                                   f"split over {ws} ranks by modelled time, keys all-gathered every step",
+                       "seq_len": cfg.L, "global_batch": 1, "chunk_rows": args.chunk, "row_ranges": ranges,
+                       "l2": "inputs larger than L2", "parallelism": f"rows{ws}"},
+            "rank0_ms_per_step": round(my_ms / args.steps, 3) if rank == 0 else None,
+            "gpu_launches": (2 * n_chunks + 1) * args.steps if T > 0 else 0,
+            "path": "all-gather of the keys (torch.distributed) + dsa_forward (C ABI) on each rank's rows",
+            "clocks": clk}
 
 
 def bench_prefill_tail(dsa, synth, args, peaks, n_rows=1024):
@@ -470,7 +627,7 @@ def bench_indexer_loss(dsa, synth, args, peaks, dense_L=32768):
                              q_pos0=0 if sparse else r0, want_p=False, kl=f.kl[r0:r1], loss=loss)
             ev.append(_rec())
         torch.cuda.synchronize()
-        st = dsa.device_status()
+        st = f.status() or dsa.device_status()
         if st != 0:
             raise RuntimeError(f"device status {st} ({stage})")
         loss_ms = _pairs_ms(ev)
@@ -543,7 +700,7 @@ def bench_decode(dsa, synth, args, peaks, cid=5):
         flush.fill_(1.0)
         stages(ev)
     torch.cuda.synchronize()
-    st = dsa.device_status()
+    st = f.status() or dsa.device_status()
     if st != 0:
         raise RuntimeError(f"decode status {st}")
     ms = float(np.median(times))
@@ -596,7 +753,7 @@ def bench_e2e(dsa, d, cfg, args, dist=None, ws=1):
     d2h = f.out.numel() * 2
 
     f()
-    n_steps = max(2, min(args.steps, 3))
+    n_steps = args.steps
     _barrier(dist)
     a = _rec()
     for _ in range(n_steps):
@@ -604,7 +761,7 @@ def bench_e2e(dsa, d, cfg, args, dist=None, ws=1):
     b = _rec()
     b.synchronize()
     ms = _max_over_ranks(dist, a.elapsed_time(b) / n_steps)
-    st = dsa.device_status()
+    st = f.status()
     if st != 0:
         raise RuntimeError(f"e2e status {st}")
     return {"value": round(aggregate_tokens_per_s(cfg.L, ws, 1, ms), 1), "unit": "tokens/s",
@@ -703,6 +860,10 @@ def main():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-fp8-peak", action="store_true", help="skip the e4m3 GEMM that measures the FP8 peak")
+    p.add_argument("--shard", default="sequences", choices=["sequences", "rows"],
+                   help="N > 1: one 128K sequence per rank (weak scaling), or one sequence split by query rows "
+                        "over the ranks (strong scaling)")
     args = p.parse_args()
     args.warmup = max(3, args.warmup)
     dist, rank, ws, _ = _dist()
