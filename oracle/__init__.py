@@ -22,6 +22,9 @@ address; sections are the pages' own numbering):
   * indexer training loss: target p = head-summed attention probabilities over
       the set, L1-normalised, and KL(p || Softmax(I)) (same page, §2.3.1 over all
       s <= t in the dense warm-up, §2.3.2 over the selected set S_t).
+  * backward of the sparse attention over a fixed selection (dq, and the latent-row
+      gradient summed over every token that selected the row): the sparse training
+      stage optimises the main model through DSA (same page, §2.3.2).
   * dense causal attention over every row s <= t: the computation DSA replaces,
       which vpshk.cn/20260227158.html and 10100.com/article/43188788 §1 compare
       DSA's cost against.
@@ -37,5 +40,6 @@ brute-force enumeration and closed forms.
 from .dsa import (  # noqa: F401
     e4m3_to_f64, bf16_bits_to_f64, indexer_row, indexer_scores, topk_row, topk_rows,
     attention_row, dense_causal_row, indexer_kl_row, indexer_loss_prefill_row, prefill_row, prefill_rows, decode_row, decode_gather,
-    selected_pairs, causal_pairs, index_sets_match, attention_error,
+    selected_pairs, causal_pairs, index_sets_match, attention_error, attention_row_backward,
+    sparse_attention_backward,
 )

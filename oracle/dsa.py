@@ -211,6 +211,71 @@ def indexer_loss_prefill_row(inp: dict, t: int, k: int, scale: float, q_pos0: in
 
 
 # ----------------------------------------------------------------------------
+# Backward of the sparse attention over a fixed selection  ([digest] §2.3.2: in
+# the sparse training stage the main model is optimised through DSA, i.e. the
+# gradient flows through the attention over the selected rows S_t)
+# ----------------------------------------------------------------------------
+
+
+def _to_f64(x) -> np.ndarray:
+    """bf16 values (torch bf16 or their uint16 bit patterns) decoded exactly; other floats as they are."""
+    a = _as_np(x)
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f64(a)
+    return np.asarray(a, dtype=np.float64)
+
+
+def attention_row_backward(q_t, latent_rows, do_t, scale: float, d_value: int = 512):
+    """Gradients of one token's sparse attention with respect to its query and the selected rows.
+
+    Forward (attention_row): z[h,s] = scale * q[h] . c[s], p = softmax_s(z), o[h] = sum_s p[h,s] c[s, :d_value].
+    With the output gradient do [H, d_value], by the chain rule through the softmax:
+        dp[h,s] = do[h] . c[s, :d_value]
+        dz[h,s] = p[h,s] * (dp[h,s] - sum_s' p[h,s'] dp[h,s'])      (the sum equals do[h] . o[h])
+        dq[h]   = scale * sum_s dz[h,s] c[s]
+        dc[s]   = scale * sum_h dz[h,s] q[h]  +  [sum_h p[h,s] do[h], 0]   (key role + value role)
+    q_t [H, 576], latent_rows [n, 576], do_t [H, d_value]: bf16 (decoded exactly) or float arrays.
+    Returns (dq [H, 576], dc [n, 576]) in float64; n == 0 gives zeros and an empty dc.
+    """
+    q = _to_f64(q_t)
+    c = _to_f64(latent_rows)
+    do = _to_f64(do_t)
+    H = q.shape[0]
+    if c.shape[0] == 0:
+        return np.zeros_like(q), np.zeros((0, q.shape[1]))
+    z = scale * (q @ c.T)                                   # [H, n]
+    e = np.exp(z - z.max(axis=1, keepdims=True))
+    p = e / e.sum(axis=1, keepdims=True)
+    v = c[:, :d_value]
+    dp = do @ v.T                                           # [H, n]
+    dz = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+    dq = scale * (dz @ c)                                   # [H, 576]
+    dc = scale * (dz.T @ q)                                 # [n, 576]
+    dc[:, :d_value] += p.T @ do
+    assert dq.shape == (H, q.shape[1])
+    return dq, dc
+
+
+def sparse_attention_backward(q, kv, idx, do, scale: float, d_value: int = 512):
+    """Gradients of the sparse attention of several tokens over their selections.
+
+    q [T, H, 576], kv [S, 576], idx [T, k] (positions, -1 = empty slot; a position may appear in
+    many rows), do [T, H, d_value].  Returns (dq [T, H, 576], dkv [S, 576]): dkv[s] sums the row
+    gradient of every token whose selection holds s.
+    """
+    kv_np = _as_np(kv)
+    idx = np.asarray(_as_np(idx), dtype=np.int64)
+    T = idx.shape[0]
+    dq = np.zeros((T,) + tuple(_as_np(q).shape[1:]))
+    dkv = np.zeros((kv_np.shape[0], kv_np.shape[1]))
+    for t in range(T):
+        sel = idx[t][idx[t] >= 0]
+        dq[t], dc = attention_row_backward(q[t], kv_np[sel], do[t], scale, d_value)
+        np.add.at(dkv, sel, dc)
+    return dq, dkv
+
+
+# ----------------------------------------------------------------------------
 # Whole forward, one query row at a time
 # ----------------------------------------------------------------------------
 

@@ -453,3 +453,89 @@ def test_indexer_loss_sparse_path_scrambled_selection_against_torch_and_scipy():
     # misaligned scores (the same positions' scores rolled by one slot) change the KL
     I_bad = np.roll(I_ref, 1)
     assert abs(rel_entr(p_ref, softmax(I_bad)).sum() - got["kl"]) > 1e-6
+
+
+# ---------------------------------------------------------------- attention backward
+
+def _sdpa_grads(q, kv, idx, do, scale):
+    """dq and d(latent rows) from torch autograd in float64 through SDPA with a boolean mask built
+    from the selection (MQA: one latent row per position, keys = all 576 dims, values = first 512)."""
+    T, H, D = q.shape
+    S = kv.shape[0]
+    qq = q.double().clone().requires_grad_(True)
+    kk = kv.double().clone().requires_grad_(True)
+    mask = torch.zeros(T, S, dtype=torch.bool)
+    for t in range(T):
+        sel = idx[t][idx[t] >= 0]
+        mask[t, sel] = True
+    out = F.scaled_dot_product_attention(qq.transpose(0, 1)[None], kk[None, None].expand(1, H, S, D),
+                                         kk[:, :512][None, None].expand(1, H, S, 512),
+                                         attn_mask=mask[None, None], scale=scale)        # [1, H, T, 512]
+    out[0].transpose(0, 1).backward(do.double())
+    return qq.grad.numpy(), kk.grad.numpy()
+
+
+def test_attention_backward_matches_torch_autograd_through_masked_sdpa():
+    g = torch.Generator().manual_seed(51)
+    T, H, S, k, scale = 6, 5, 40, 9, 0.06
+    q = torch.randn(T, H, 576, generator=g).to(torch.bfloat16)
+    kv = torch.randn(S, 576, generator=g).to(torch.bfloat16)
+    do = torch.randn(T, H, 512, generator=g).to(torch.bfloat16)
+    idx = torch.full((T, k + 3), -1, dtype=torch.int64)
+    for t in range(T):
+        n = [k, 3, k, 1, k, 7][t]
+        idx[t, :n] = torch.randperm(S, generator=g)[:n]      # overlapping selections, scrambled order
+    dq, dkv = oracle.sparse_attention_backward(q, kv, idx.numpy(), do, scale)
+    dq_ref, dkv_ref = _sdpa_grads(q, kv, idx, do, scale)
+    np.testing.assert_allclose(dq, dq_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dkv, dkv_ref, rtol=1e-10, atol=1e-12)
+    # rows never selected get no gradient; the value role only touches the first 512 dims
+    unused = np.setdiff1d(np.arange(S), idx[idx >= 0].numpy())
+    assert np.all(dkv[unused] == 0)
+
+
+def test_attention_backward_matches_finite_differences():
+    # float64 inputs (the oracle takes them as they are), central differences of L = <do, o>
+    rng = np.random.default_rng(52)
+    H, n, scale = 3, 7, 0.3
+    q = rng.standard_normal((H, 576))
+    c = rng.standard_normal((n, 576))
+    do = rng.standard_normal((H, 512))
+    dq, dc = oracle.attention_row_backward(q, c, do, scale)
+
+    def loss(qx, cx):
+        z = scale * (qx @ cx.T)
+        p = np.exp(z - z.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        return float(np.sum(do * (p @ cx[:, :512])))
+
+    eps = 1e-6
+    for (h, d) in [(0, 0), (1, 300), (2, 575), (0, 511), (2, 512)]:
+        e = np.zeros_like(q)
+        e[h, d] = eps
+        fd = (loss(q + e, c) - loss(q - e, c)) / (2 * eps)
+        assert abs(fd - dq[h, d]) <= 1e-6 * max(1.0, abs(fd)), (h, d, fd, dq[h, d])
+    for (s, d) in [(0, 0), (3, 100), (6, 511), (6, 512), (1, 575)]:
+        e = np.zeros_like(c)
+        e[s, d] = eps
+        fd = (loss(q, c + e) - loss(q, c - e)) / (2 * eps)
+        assert abs(fd - dc[s, d]) <= 1e-6 * max(1.0, abs(fd)), (s, d, fd, dc[s, d])
+
+
+def test_attention_backward_special_cases():
+    g = torch.Generator().manual_seed(53)
+    q = torch.randn(4, 576, generator=g).to(torch.bfloat16)
+    c = torch.randn(1, 576, generator=g).to(torch.bfloat16)
+    do = torch.randn(4, 512, generator=g).to(torch.bfloat16)
+    # one selected row: the softmax is constant (p = 1), so dq = 0 and dc = [sum_h do_h, 0]
+    dq, dc = oracle.attention_row_backward(q, c, do, 0.1)
+    assert np.all(dq == 0)
+    np.testing.assert_allclose(dc[0, :512], do.double().sum(0).numpy(), rtol=1e-14)
+    assert np.all(dc[0, 512:] == 0)
+    # an empty selection: no gradient at all
+    dq, dc = oracle.attention_row_backward(q, c[:0], do, 0.1)
+    assert np.all(dq == 0) and dc.shape == (0, 576)
+    # a zero output gradient gives zero gradients
+    c2 = torch.randn(5, 576, generator=g).to(torch.bfloat16)
+    dq, dc = oracle.attention_row_backward(q, c2, torch.zeros(4, 512), 0.1)
+    assert np.all(dq == 0) and np.all(dc == 0)
