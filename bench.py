@@ -296,6 +296,13 @@ def run_ours(args, dist, rank, ws):
         return bench_dense_curve(dsa, synth, args, peaks)
     if args.workload == "indexer_loss":
         return bench_indexer_loss(dsa, synth, args, peaks)
+    if args.workload.startswith("backward"):
+        res = bench_backward(dsa, synth, args, peaks, L=131072 if args.workload == "backward128k" else 4096)
+        return {"metric": "sparse attention backward tokens/s", "value": res["tokens_per_s"], "unit": "tokens/s",
+                "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16 (fp32 accum, fp32 dkv atomics)", "data": "synthetic",
+                "config": {"workload": res["workload"]}, "backward": res}
     if args.shard == "rows":
         return bench_prefill_rows(dsa, synth, args, peaks, dist, rank, ws)
     cid = {"prefill128k": 4, "prefill4k": 2}[args.workload]
@@ -468,6 +475,65 @@ def bench_prefill_rows(dsa, synth, args, peaks, dist, rank, ws):
             "gpu_launches": (2 * n_chunks + 1) * args.steps if T > 0 else 0,
             "path": "all-gather of the keys (torch.distributed) + dsa_forward (C ABI) on each rank's rows",
             "clocks": clk}
+
+
+def backward_work(L, H, k):
+    """Algorithmic work of the sparse-attention backward over a causal prefill's selections."""
+    sel = sum(min(t + 1, k) for t in range(min(L, k))) + max(0, L - k) * k
+    # per (token, key): S and dq over 576 dims, dP and dv over 512, dk over 576 -> 2 H (576 + 512 + 576 + 576 + 512)
+    return dict(flop=2.0 * H * 2752 * sel, selected=sel,
+                atomic_bytes=4.0 * 576 * sel,                        # fp32 adds into dkv, per (token, key)
+                stream_bytes=L * H * (576 + 512 + 512 + 576) * 2.0)  # q, o, do read and dq written
+
+
+def bench_backward(dsa, synth, args, peaks, L=4096):
+    """The backward of the sparse attention over one prefill's selections (k=2048, H=128): the forward
+    runs once (dsa_forward: indexer, top-k, attention) to give the selection, O and lse; the timed
+    step is dsa_sparse_attn_backward over every row, with a random output gradient."""
+    cfg = synth.config(4, L=L)
+    d = synth.prefill_inputs(cfg, device="cuda")
+    idx = torch.empty((L, cfg.k), dtype=torch.int32, device="cuda")
+    lse = torch.empty((L, cfg.H), dtype=torch.float32, device="cuda")
+    f = dsa.Forward.prefill(d, cfg.k, cfg.scale, chunk_rows=min(args.chunk, L), lse=lse, idx=idx)
+    f()
+    if f.status() != 0:
+        raise RuntimeError("forward status")
+    g = torch.Generator(device="cuda").manual_seed(5)
+    do = torch.randn((L, cfg.H, 512), generator=g, device="cuda").to(torch.bfloat16)
+    dq = torch.empty((L, cfg.H, 576), dtype=torch.bfloat16, device="cuda")
+    dkv = torch.zeros((L, 576), dtype=torch.float32, device="cuda")
+    w = dsa.status_word()
+
+    def step():
+        dkv.zero_()
+        dsa.sparse_attn_backward(d["q"], d["kv"], idx, cfg.scale, f.out, do, lse, dq=dq, dkv=dkv, status=w)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(args.steps):
+        dkv.zero_()
+        ev.append(_rec())
+        dsa.sparse_attn_backward(d["q"], d["kv"], idx, cfg.scale, f.out, do, lse, dq=dq, dkv=dkv, status=w)
+        ev.append(_rec())
+    torch.cuda.synchronize()
+    st = dsa.read_status(w)
+    if st != 0:
+        raise RuntimeError(f"backward status {st}")
+    ms = _pairs_ms(ev) / args.steps
+    wk = backward_work(L, cfg.H, cfg.k)
+    tf = wk["flop"] / (ms * 1e-3) / 1e12
+    res = {"L": L, "ms": round(ms, 3), "tokens_per_s": round(L / (ms * 1e-3), 1),
+           "workload": f"backward of the sparse attention over a prefill L={L}, k=2048, H=128 (dq bf16, dkv fp32)",
+           "kernel": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
+                      "frac": round(tf / peaks["bf16_sus"], 4), "peak_source": f"{peaks['src']} bf16 sustained",
+                      "work": "2 H (576 + 512 + 576 + 576 + 512) FLOP per selected (token, key) pair"},
+           "atomic_GBps": round(wk["atomic_bytes"] / (ms * 1e-3) / 1e9, 1),
+           "launches": 1}
+    del d, f, do, dq, dkv
+    torch.cuda.empty_cache()
+    return res
 
 
 def bench_prefill_tail(dsa, synth, args, peaks, n_rows=1024):
@@ -853,7 +919,7 @@ def main():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--chunk", type=int, default=8192)
     p.add_argument("--workload", default="prefill128k", choices=["prefill128k", "prefill4k", "prefill128k_tail", "decode", "decode32k",
-                                                       "dense_curve", "indexer_loss"],
+                                                       "dense_curve", "indexer_loss", "backward", "backward128k"],
                    help="the others run single pieces (used for profiler captures)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--e2e-chunk", type=int, default=2048, help="query rows per chunk of the host-buffer pipeline")

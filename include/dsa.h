@@ -236,6 +236,35 @@ dsa_status_t dsa_indexer_loss(const uint16_t* q, const uint16_t* kv, int64_t n_k
                               const float* scores, int64_t ld, float* p, float* kl, double* loss_acc,
                               int32_t* dev_status, dsa_stream_t stream);
 
+/*
+ * dsa_sparse_attn_backward — gradients of dsa_sparse_attn over a fixed selection
+ * (freezhihu.org/question/1978819912970555965 §2.3.2: the sparse training stage optimises the
+ * main model through the attention over the selected rows S_t).
+ *
+ * With z[h,s] = scale * q[t,h,:] . c_s, p = softmax_s(z) over S_t and o = sum_s p c_s[0:512] (the
+ * forward), and do = dL/do:
+ *     ds[h,s] = p[h,s] * (do[t,h,:] . c_s[0:512] - do[t,h,:] . o[t,h,:])
+ *     dq[t,h,:]  = scale * sum_{s in S_t} ds[h,s] c_s
+ *     dkv[s,:]  += scale * sum_h ds[h,s] q[t,h,:]  +  [sum_h p[h,s] do[t,h,:], 0]   for every t with s in S_t
+ * p is recomputed from q, kv and the forward's lse; products on the tensor cores with bf16 inputs
+ * (p and ds are rounded to bf16 before their products) and fp32 accumulation.
+ *
+ *   q, kv, n_kv_rows, idx, T, H, k, scale: as in dsa_sparse_attn (contiguous kv only)
+ *   out   [T, H, 512] bf16: the forward's output (for do . o), 16-byte aligned
+ *   dout  [T, H, 512] bf16: gradient of the output, 16-byte aligned
+ *   lse   [T, H] fp32: the forward's lse output
+ *   dq    [T, H, 576] bf16 output, 16-byte aligned (rows of a token with no valid slot are zero)
+ *   dkv   [n_kv_rows, 576] fp32: the latent-row gradients are ADDED to it (the caller zeroes it),
+ *         with atomic adds, so the summation order over tokens is not fixed
+ *   dev_status  device status word, or NULL
+ * Errors as dsa_sparse_attn (an out-of-range position is skipped and reported as
+ * DSA_ERR_DEVICE_RANGE).
+ */
+dsa_status_t dsa_sparse_attn_backward(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows,
+                                      const int32_t* idx, int T, int H, int k, float scale,
+                                      const uint16_t* out, const uint16_t* dout, const float* lse,
+                                      uint16_t* dq, float* dkv, int32_t* dev_status, dsa_stream_t stream);
+
 /* Forward modes. */
 enum { DSA_MODE_PREFILL = 0, DSA_MODE_DECODE = 1 };
 

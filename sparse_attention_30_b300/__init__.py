@@ -26,7 +26,7 @@ EXPORTS = ("dsa_status_string", "dsa_version", "dsa_index", "dsa_index_paged", "
            "dsa_decode_noalloc", "dsa_decode_noalloc_capacity", "dsa_sparse_attn_split_workspace_size",
            "dsa_sparse_attn_split", "dsa_prefill_host_workspace_size", "dsa_prefill_host",
            "dsa_dense_causal_attn", "dsa_indexer_loss", "dsa_wait_limit_ns", "dsa_forward_loss_workspace_size",
-           "dsa_forward_loss", "dsa_status")
+           "dsa_forward_loss", "dsa_status", "dsa_sparse_attn_backward")
 
 
 class DSAError(RuntimeError):
@@ -83,6 +83,7 @@ def _load():
         "dsa_forward_loss_workspace_size": ([ctypes.POINTER(ForwardArgs), I], ctypes.c_size_t),
         "dsa_forward_loss": ([ctypes.POINTER(ForwardArgs), I, P, P, P, ctypes.c_size_t, P], I),
         "dsa_prefill_host": ([ctypes.POINTER(ForwardArgs), P, ctypes.c_size_t, P], I),
+        "dsa_sparse_attn_backward": ([P, P, I64, P, I, I, I, F, P, P, P, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -246,6 +247,27 @@ def indexer_loss(q, kv, lse, scores, scale, idx=None, q_pos0=0, p=None, kl=None,
                                 _stream(q)),
            "dsa_indexer_loss")
     return p, kl, loss
+
+
+def sparse_attn_backward(q, kv, idx, scale, out, dout, lse, dq=None, dkv=None, status=None):
+    """Gradients of sparse_attn over the fixed selection idx (dsa_sparse_attn_backward).
+    q [T, H, 576] / kv [S, 576] / out, dout [T, H, 512] bf16, lse [T, H] fp32 from the forward.
+    Returns (dq [T, H, 576] bf16, dkv [S, 576] fp32); dkv is added to when passed (zeroed otherwise)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv, torch.bfloat16, "kv", 2)
+    _need(idx, torch.int32, "idx", 2)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(dout, torch.bfloat16, "dout", 3)
+    _need(lse, torch.float32, "lse", 2)
+    T, H, _ = q.shape
+    if dq is None:
+        dq = torch.empty((T, H, 576), dtype=torch.bfloat16, device=q.device)
+    if dkv is None:
+        dkv = torch.zeros((kv.shape[0], 576), dtype=torch.float32, device=q.device)
+    _check(lib.dsa_sparse_attn_backward(_ptr(q), _ptr(kv), kv.shape[0], _ptr(idx), T, H, idx.shape[1], float(scale),
+                                        _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dkv), _ptr(status),
+                                        _stream(q)), "dsa_sparse_attn_backward")
+    return dq, dkv
 
 
 def decode_split(B: int) -> int:

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libdsa.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["api.cu", "indexer.cu", "indexer_paged.cu", "topk.cu", "sparse_attn.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "indexer.cu", "indexer_paged.cu", "topk.cu", "sparse_attn.cu", "sparse_attn_bwd.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
 

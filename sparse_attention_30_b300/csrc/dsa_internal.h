@@ -99,6 +99,25 @@ struct AttnArgs {
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- sparse attention backward
+
+struct BwdArgs {
+  const uint16_t* q;          // [T, H, 576] bf16
+  const uint16_t* kv;         // [n_kv_rows, 576] bf16
+  int64_t n_kv_rows;
+  const int32_t* idx;         // [T, k]
+  int T, H, k;
+  float scale;                // softmax scale
+  const uint16_t* out;        // [T, H, 512] bf16: the forward's output
+  const uint16_t* dout;       // [T, H, 512] bf16: gradient of the output
+  const float* lse;           // [T, H] natural-log normalisers of the forward
+  uint16_t* dq;               // [T, H, 576] bf16
+  float* dkv;                 // [n_kv_rows, 576] fp32, added to
+  int* status;
+  uint64_t limit_ns;
+};
+cudaError_t launch_sparse_attn_bwd(const BwdArgs& a, cudaStream_t stream);
+
 // ---------------------------------------------------------------- host-side argument checks (api.cu)
 
 // Each returns DSA_OK, or the status the public call returns before launching anything.

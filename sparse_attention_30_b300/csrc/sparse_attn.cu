@@ -29,11 +29,14 @@
 // chains are issue-bound rather than tensor-bound.
 #include <cuda_bf16.h>
 
+#include "attn_common.cuh"
 #include "dsa_internal.h"
 #include "dsa_ptx.cuh"
 
 namespace dsa {
 namespace {
+
+using namespace attn;
 
 constexpr int kProdWarps = 12;                 // warps 1..12 gather
 constexpr int kProducers = kProdWarps * 32;
@@ -76,17 +79,6 @@ constexpr int kItemReaders0 = 1 + kProdWarps + 4, kItemReaders1 = kItemReaders0 
 static_assert(kColS + kSBufs * kKT <= kTmemCols, "rank 0 TMEM budget");
 static_assert(kQBytes <= kKStages * kKStageBytes, "Q is staged in rank 0's K ring");
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Physical latent row of position s for row t, or -1 if the slot is empty or out of range.
 __device__ __forceinline__ int64_t latent_row(const AttnArgs& a, int t, int32_t s, bool* range_err) {
@@ -148,27 +140,6 @@ __device__ __forceinline__ bool read_item(Bars& bars, const Item* sched, int j, 
   return true;
 }
 
-// First empty slot of a selection row (valid slots come first), by the whole warp: each round
-// probes 32 evenly spaced positions of the open interval, so k = 2048 takes three dependent loads.
-__device__ int first_empty_slot(const int32_t* idx_row, int k) {
-  const int lane = threadIdx.x & 31;
-  int lo = 0, hi = k;  // every slot below lo is valid; the first empty one is in [lo, hi]
-  while (hi - lo > 32) {
-    const int step = (hi - lo + 31) / 32;
-    const int p = lo + lane * step;
-    const bool neg = p < hi && __ldg(idx_row + p) < 0;
-    const unsigned m = __ballot_sync(0xffffffffu, neg);
-    const int f = m ? __ffs(m) - 1 : 32;
-    if (f == 0) return lo;
-    const int nlo = lo + (f - 1) * step + 1;
-    hi = f < 32 ? lo + f * step : hi;
-    lo = nlo;
-  }
-  const int p = lo + lane;
-  const unsigned m = __ballot_sync(0xffffffffu, p < hi && __ldg(idx_row + p) < 0);
-  return m ? lo + __ffs(m) - 1 : hi;
-}
-
 // Gather of tile i: `nblk` 64-dim blocks (from latent dim 0) of each of the 64 selected rows into
 // a 128B-swizzled stage.  Producer warp pw copies whole rows pw, pw + 12, ...: the tile's positions
 // are read once (two per lane) and row addresses are broadcast with shuffles.  An empty or
@@ -196,29 +167,6 @@ __device__ __forceinline__ void gather_rows(const AttnArgs& a, int t, const int3
       const int cc = lane + 32 * j;
       if (cc < kChunks)
         ptx::cp_async16_n<16>(drow + (cc >> 3) * kBlockBytes + (((cc & 7) ^ (r & 7)) << 4), src + cc * 8);
-    }
-  }
-}
-
-// Transpose of N x N 16-byte chunks among N consecutive lanes: lane i's v[k] (chunk k of its
-// row) becomes chunk i of lane k's row, so that N lanes then store one row's N chunks together.
-template <int N>
-__device__ __forceinline__ void transpose_chunks(uint4 (&v)[N]) {
-  const int i = threadIdx.x & (N - 1);
-#pragma unroll
-  for (int sh = N / 2; sh >= 1; sh >>= 1) {
-    const bool up = (i & sh) != 0;
-#pragma unroll
-    for (int k = 0; k < N; ++k) {
-      if (k & sh) continue;
-      const uint4 send = up ? v[k] : v[k ^ sh];
-      uint4 recv;
-      recv.x = __shfl_xor_sync(0xffffffffu, send.x, sh);
-      recv.y = __shfl_xor_sync(0xffffffffu, send.y, sh);
-      recv.z = __shfl_xor_sync(0xffffffffu, send.z, sh);
-      recv.w = __shfl_xor_sync(0xffffffffu, send.w, sh);
-      if (up) v[k] = recv;
-      else v[k ^ sh] = recv;
     }
   }
 }
