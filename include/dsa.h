@@ -254,8 +254,8 @@ dsa_status_t dsa_indexer_loss(const uint16_t* q, const uint16_t* kv, int64_t n_k
  *   dout  [T, H, 512] bf16: gradient of the output, 16-byte aligned
  *   lse   [T, H] fp32: the forward's lse output
  *   dq    [T, H, 576] bf16 output, 16-byte aligned (rows of a token with no valid slot are zero)
- *   dkv   [n_kv_rows, 576] fp32: the latent-row gradients are ADDED to it (the caller zeroes it),
- *         with atomic adds, so the summation order over tokens is not fixed
+ *   dkv   [n_kv_rows, 576] fp32, 16-byte aligned: the latent-row gradients are ADDED to it (the
+ *         caller zeroes it), with atomic adds, so the summation order over tokens is not fixed
  *   dev_status  device status word, or NULL
  * Errors as dsa_sparse_attn (an out-of-range position is skipped and reported as
  * DSA_ERR_DEVICE_RANGE).

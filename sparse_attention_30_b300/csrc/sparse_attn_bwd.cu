@@ -74,7 +74,7 @@ struct Bars {
   // rank 0
   uint64_t k_full[kStages], k_empty[kStages], s_full[2], s_empty[2], q_full, q_free;
   uint64_t p_empty[2];      // credit from rank 1: its P slot may be overwritten
-  uint64_t ds_full;         // rank 1's 128 row threads wrote dS into this CTA's slot
+  uint64_t ds_full;         // rank 1's bulk copy of dS into this CTA's slot landed (armed with its bytes)
   uint64_t ds_consumed;     // this CTA's products reading that slot completed
   // rank 1
   uint64_t v_full[kStages], v_empty[kStages], dp_full[2], dp_empty[2], do_full, do_free;
@@ -131,16 +131,21 @@ __device__ __forceinline__ uint64_t desc_sw64_mn(uint32_t addr) { return ptx::sm
 // Byte offset of 16-byte chunk c (0..3) of row r in a [rows x 64 B] 64B-swizzled slot.
 __device__ __forceinline__ uint32_t slot_off(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
 
-// Gather of tile i: NBLK 64-dim blocks of each of its 32 selected rows into a 128B-swizzled stage.
-// Producer warp pw copies rows pw, pw + 8, pw + 16, pw + 24; an empty or out-of-range slot copies
-// `fallback` (a row the token attends; its key is masked to P = 0 downstream).
+// Selection entry of this lane's key in tile i of a row (-1 past the row's slots).
+__device__ __forceinline__ int32_t sel_entry(const BwdArgs& a, const int32_t* idx_row, int i) {
+  const int slot = i * kKT + (threadIdx.x & 31);
+  return slot < a.k ? __ldg(idx_row + slot) : -1;
+}
+
+// Gather of a tile: NBLK 64-dim blocks of each of its 32 selected rows into a 128B-swizzled stage;
+// lane l holds the selection entry s of key l.  Producer warp pw copies rows pw, pw + 8, pw + 16,
+// pw + 24; an empty or out-of-range slot copies `fallback` (a row the token attends; its key is
+// masked to P = 0 downstream).
 template <int NBLK>
-__device__ __forceinline__ void gather_tile(const BwdArgs& a, const int32_t* idx_row, int i, uint32_t dst, int pw,
-                                            int lane, int64_t fallback) {
+__device__ __forceinline__ void gather_tile(const BwdArgs& a, int32_t s, uint32_t dst, int pw, int lane,
+                                            int64_t fallback) {
   constexpr int kChunks = NBLK * 8;
-  const int slot = i * kKT + lane;
   bool unused = false;
-  const int32_t s = slot < a.k ? __ldg(idx_row + slot) : -1;
   const int64_t pr = sel_row(a, s, &unused);
   const uint16_t* base = a.kv + (pr < 0 ? fallback : pr) * kDL;
   for (int r = pw; r < kKT; r += kProdWarps) {
@@ -185,8 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::mbar_init(baddr(bars.q_full), 1);
       ptx::mbar_init(baddr(bars.q_free), 1);
-      ptx::mbar_init(baddr(bars.ds_full), 128);
+      ptx::mbar_init(baddr(bars.ds_full), 1);
       ptx::mbar_init(baddr(bars.ds_consumed), 1);
+      ptx::mbar_arrive_expect_tx(baddr(bars.ds_full), kSlot);  // armed for the first copy
     } else {
       for (int s = 0; s < kStages; ++s) {
         ptx::mbar_init(baddr(bars.v_full[s]), kProducers);
@@ -387,21 +393,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t fallback = sel_row(a, __ldg(idx_row), &range_err);
       if (fallback < 0) fallback = 0;
       bool ok = true;
+      int32_t s_next = sel_entry(a, idx_row, 0);  // each tile's entries are loaded a tile ahead
       for (int i = 0; i < n; ++i) {
         const int gi = g + i, st = gi % kStages;
+        const int32_t s_cur = s_next;
+        if (i + 1 < n) s_next = sel_entry(a, idx_row, i + 1);
         if (rank == 0) {
           if (!warp_wait(baddr(bars.k_empty[st]), ((gi / kStages) & 1) ^ 1, abort_flag, a)) {
             ok = false;
             break;
           }
-          gather_tile<9>(a, idx_row, i, sbase + kOffK + st * kKStage, pw, lane, fallback);
+          gather_tile<9>(a, s_cur, sbase + kOffK + st * kKStage, pw, lane, fallback);
           ptx::cp_async_arrive_noinc(baddr(bars.k_full[st]));
         } else {
           if (!warp_wait(baddr(bars.v_empty[st]), ((gi / kStages) & 1) ^ 1, abort_flag, a)) {
             ok = false;
             break;
           }
-          gather_tile<8>(a, idx_row, i, sbase + kOffV + st * kVStage, pw, lane, fallback);
+          gather_tile<8>(a, s_cur, sbase + kOffV + st * kVStage, pw, lane, fallback);
           ptx::cp_async_arrive_noinc(baddr(bars.v_full[st]));
         }
       }
@@ -424,8 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n == 0) continue;
         const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.k;
         const float lse2 = h < a.H ? a.lse[static_cast<int64_t>(t) * a.H + h] * 1.4426950408889634f : INFINITY;
+        int32_t s_next = sel_entry(a, idx_row, 0);
         for (int i = 0; i < n; ++i) {
           const int gi = g + i, sb = gi & 1, ps = gi & 1;
+          const int32_t sidx = s_next;
+          if (i + 1 < n) s_next = sel_entry(a, idx_row, i + 1);
           if (!warp_wait(baddr(bars.s_full[sb]), (gi >> 1) & 1, abort_flag, a)) {
             ok = false;
             break;
@@ -436,8 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_wait_ld();
           ptx::tc_fence_before();
           ptx::mbar_arrive(baddr(bars.s_empty[sb]));
-          const int slot = i * kKT + lane;
-          const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
           const uint32_t vm = __ballot_sync(0xffffffffu, sel_row(a, sidx, &range_err) >= 0);
           uint32_t pk[16];
 #pragma unroll
@@ -464,16 +474,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq;
       }
     } else {
-      // ---- dS = P (dP - D) into the local slot and rank 0's slot
+      // ---- dS = P (dP - D) into the local slot and rank 0's slot.  These 128 threads meet at named
+      // barriers (unbounded), so they leave only together: a failed wait is voted on at the next
+      // barrier instead of breaking out alone.
       const uint32_t peer_ds = ptx::map_to_rank(sbase + kOffDs0, peer);
       const uint8_t* dos = smem + kOffDO + h * 128;
       for (int t = cl; ok && t < a.T; t += n_cl) {
         const int n = tiles_of(a, t);
         if (n == 0) continue;
         // D = dO[h] . O[h] (dO from shared memory, the forward's O from global memory)
-        if (!warp_wait(baddr(bars.do_full), nq & 1, abort_flag, a)) break;
+        const bool d_ok = warp_wait(baddr(bars.do_full), nq & 1, abort_flag, a);
         float D = 0.f;
-        if (h < a.H) {
+        if (d_ok && h < a.H) {
           const uint4* orow = reinterpret_cast<const uint4*>(a.out + (static_cast<int64_t>(t) * a.H + h) * kDV);
 #pragma unroll 2
           for (int b = 0; b < 8; ++b) {
@@ -494,36 +506,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < n; ++i) {
           const int gi = g + i, pb = gi & 1, ps = gi & 1;
-          if (!warp_wait(baddr(bars.dp_full[pb]), (gi >> 1) & 1, abort_flag, a)) {
-            ok = false;
-            break;
-          }
+          bool fail = !d_ok;
           uint32_t dv[32];
-          ptx::tc_fence_after();
-          ptx::tmem_ld32(tmem + kColDp + pb * kKT + lane_base, dv);
-          ptx::tmem_wait_ld();
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(baddr(bars.dp_empty[pb]));
-          if (!warp_wait_cluster(baddr(bars.p_full[ps]), (gi >> 1) & 1, abort_flag, a)) {
-            ok = false;
-            break;
+          if (!fail && warp_wait(baddr(bars.dp_full[pb]), (gi >> 1) & 1, abort_flag, a)) {
+            ptx::tc_fence_after();
+            ptx::tmem_ld32(tmem + kColDp + pb * kKT + lane_base, dv);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(baddr(bars.dp_empty[pb]));
+          } else {
+            fail = true;
           }
-          const uint8_t* prow = smem + kOffP + ps * kSlot;
           uint32_t pk[16];
+          if (!fail && warp_wait_cluster(baddr(bars.p_full[ps]), (gi >> 1) & 1, abort_flag, a)) {
+            const uint8_t* prow = smem + kOffP + ps * kSlot;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 x = *reinterpret_cast<const uint4*>(prow + slot_off(h, c));
-            pk[4 * c] = x.x; pk[4 * c + 1] = x.y; pk[4 * c + 2] = x.z; pk[4 * c + 3] = x.w;
+            for (int c = 0; c < 4; ++c) {
+              const uint4 x = *reinterpret_cast<const uint4*>(prow + slot_off(h, c));
+              pk[4 * c] = x.x; pk[4 * c + 1] = x.y; pk[4 * c + 2] = x.z; pk[4 * c + 3] = x.w;
+            }
+            ptx::mbar_arrive(baddr(bars.p_consumed[ps]));
+          } else {
+            fail = true;
           }
-          ptx::mbar_arrive(baddr(bars.p_consumed[ps]));
+          if (!fail) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[e]));
-            pk[e] = pack_bf16(p.x * (__uint_as_float(dv[2 * e]) - D), p.y * (__uint_as_float(dv[2 * e + 1]) - D));
+            for (int e = 0; e < 16; ++e) {
+              const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[e]));
+              pk[e] = pack_bf16(p.x * (__uint_as_float(dv[2 * e]) - D), p.y * (__uint_as_float(dv[2 * e + 1]) - D));
+            }
           }
-          // local slot (for rank 1's dq product), then rank 0's slot
-          bool w_ok = ptx::mbar_wait(baddr(bars.dsl_empty[ps]), ((gi >> 1) & 1) ^ 1, abort_flag, a.status, a.limit_ns);
-          if (!__all_sync(0xffffffffu, w_ok)) {
+          // The local slot feeds this CTA's dq product; one bulk copy of it then feeds rank 0.  Before
+          // the slot is rewritten, its products (dsl_empty) and the copy of two tiles ago (the
+          // copying thread's bulk group) must have read it.
+          if (!fail)
+            fail = !ptx::mbar_wait(baddr(bars.dsl_empty[ps]), ((gi >> 1) & 1) ^ 1, abort_flag, a.status, a.limit_ns);
+          if (h == 0) ptx::bulk_wait_read<1>();
+          if (ptx::named_sync_or(1, 128, fail || *abort_flag)) {
             ok = false;
             break;
           }
@@ -533,20 +552,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dsl + slot_off(h, c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           ptx::fence_proxy_async_smem();
           ptx::mbar_arrive(baddr(bars.dsl_full[ps]));
-          w_ok = ptx::mbar_wait_cluster(baddr(bars.ds_peer_empty), (gi & 1) ^ 1, abort_flag, a.status, a.limit_ns);
-          if (!__all_sync(0xffffffffu, w_ok)) {
-            ok = false;
-            break;
+          ptx::named_sync(2, 128);
+          if (h == 0) {
+            // a failed wait raises the abort flag, which the next vote picks up
+            if (ptx::mbar_wait_cluster(baddr(bars.ds_peer_empty), (gi & 1) ^ 1, abort_flag, a.status, a.limit_ns)) {
+              ptx::bulk_copy_to_cluster(peer_ds, ptx::smem_addr(dsl), kSlot, ptx::map_to_rank(baddr(bars.ds_full), peer));
+              ptx::bulk_commit();
+            }
           }
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            ptx::st_cluster_v4(peer_ds + slot_off(h, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          ptx::fence_proxy_async_cluster();
-          ptx::mbar_arrive_cluster(ptx::map_to_rank(baddr(bars.ds_full), peer));
         }
-        g += n;
-        ++nq;
+        if (ok) {
+          g += n;
+          ++nq;
+        }
       }
+      if (h == 0) ptx::bulk_wait_all<0>();  // every copy has landed in rank 0 before either CTA exits
     }
     if (range_err) atomicCAS(a.status, 0, DSA_ERR_DEVICE_RANGE);
   } else if (warp < kCreditWarp) {
@@ -570,12 +590,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.k;
+      int32_t s_next = sel_entry(a, idx_row, 0);
       for (int i = 0; ok && i < n; ++i) {
         const int gi = g + i;
-        const int slot = i * kKT + lane;
         bool unused = false;
-        const int32_t sidx = slot < a.k ? __ldg(idx_row + slot) : -1;
-        const int64_t my_row = sel_row(a, sidx, &unused);
+        const int64_t my_row = sel_row(a, s_next, &unused);
+        if (i + 1 < n) s_next = sel_entry(a, idx_row, i + 1);
         for (int j = 0; j < nblk; ++j) {
           if (!warp_wait(baddr(bars.dc_full[j]), gi & 1, abort_flag, a)) {
             ok = false;
@@ -587,12 +607,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_wait_ld();
           ptx::tc_fence_before();
           ptx::mbar_arrive(baddr(bars.dc_empty[j]));
-          const int dim = j * 128 + q4 * 32 + lane;
-          if (rank == 0 && dim >= kDL) continue;  // the padded rows of the last block (whole warps)
+          const int dim0 = j * 128 + q4 * 32;      // this warp's 32 dims (lane = dim)
+          if (rank == 0 && dim0 >= kDL) continue;  // the padded rows of the last block (whole warps)
+          // 4 x 4 transposes among groups of four lanes: afterwards lane 4g + r holds dims
+          // dim0 + 4g .. + 3 of keys 4kk + r (kk = 0..7), so each key's 4 dims go in one vector add
+          float x[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const long long r = __shfl_sync(0xffffffffu, static_cast<long long>(my_row), c);
-            if (r >= 0) atomicAdd(a.dkv + r * kDL + dim, __uint_as_float(v[c]) * fac);
+          for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]) * fac;
+          const int r4 = lane & 3;
+#pragma unroll
+          for (int sh = 2; sh >= 1; sh >>= 1) {
+            const bool up = (r4 & sh) != 0;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if (e & sh) continue;
+                const float send = up ? x[4 * kk + e] : x[4 * kk + (e ^ sh)];
+                const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
+                if (up) x[4 * kk + e] = recv;
+                else x[4 * kk + (e ^ sh)] = recv;
+              }
+            }
+          }
+          const int dim = dim0 + (lane & ~3);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const long long r = __shfl_sync(0xffffffffu, static_cast<long long>(my_row), 4 * kk + r4);
+            if (r >= 0)
+              atomicAdd(reinterpret_cast<float4*>(a.dkv + r * kDL + dim),
+                        make_float4(x[4 * kk], x[4 * kk + 1], x[4 * kk + 2], x[4 * kk + 3]));
           }
         }
       }
@@ -648,7 +692,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_to_rank(baddr(bars.ds_peer_empty), peer));
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(baddr(bars.ds_full), kSlot);  // armed for the next copy
+            ptx::mbar_arrive_cluster(ptx::map_to_rank(baddr(bars.ds_peer_empty), peer));
+          }
         } else {
           const int ps = gi & 1;
           if (!warp_wait(baddr(bars.p_consumed[ps]), (gi >> 1) & 1, abort_flag, a)) {
@@ -716,7 +763,7 @@ extern "C" dsa_status_t dsa_sparse_attn_backward(const uint16_t* q, const uint16
   if (st != DSA_OK) return st;
   if (!dout || !lse || !dq || !dkv) return DSA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(dout) & 15u) || (reinterpret_cast<uintptr_t>(dq) & 15u) ||
-      (reinterpret_cast<uintptr_t>(dkv) & 3u))
+      (reinterpret_cast<uintptr_t>(dkv) & 15u))
     return DSA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(T) * H > (1ll << 31) - 1) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
