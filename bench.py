@@ -89,7 +89,16 @@ def measure_fp8_peak(n=8192, sustain_s=2.0):
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of one kernel per unit of its work,
 # from a capture of a given build of that kernel's source.  A figure is reported only while the
 # source still hashes to the captured build; otherwise `traffic` is null.
-TRAFFIC_CAPTURES = {}
+TRAFFIC_CAPTURES = {
+    # dram__bytes.sum of one launch over the last 1024 query rows of the 128K prefill (each row against
+    # ~131K keys), per query row; the capture replays from a flushed L2, so it overstates the steady state
+    "sparse_attn": {"src": "f52ab0886cd0fae0", "bytes_per_unit": 612.1e6 / 1024,
+                    "capture": "ncu dram__bytes.sum, sparse_attn_kernel<0> over the 1024-row 128K tail, per row x rows"},
+    "indexer": {"src": "5a7e056d47d32a72", "bytes_per_unit": 539.5e6 / 1024,
+                "capture": "ncu dram__bytes.sum, indexer_kernel<64> over the 1024-row 128K tail, per row x rows"},
+    "topk": {"src": "5cbb3de9049894a9", "bytes_per_unit": 624.6e6 / 1024,
+             "capture": "ncu dram__bytes.sum, topk_kernel over the 1024-row 128K tail, per row x rows"},
+}
 
 
 def _src_hash(files):
@@ -101,8 +110,9 @@ def _src_hash(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"sparse_attn": ["sparse_attn.cu", "dsa_ptx.cuh"], "indexer": ["indexer.cu", "dsa_ptx.cuh"],
-                  "topk": ["topk.cu"]}
+KERNEL_SOURCES = {"sparse_attn": ["sparse_attn.cu", "attn_common.cuh", "dsa_ptx.cuh", "dsa_internal.h"],
+                  "indexer": ["indexer.cu", "dsa_ptx.cuh", "dsa_internal.h"],
+                  "topk": ["topk.cu", "dsa_ptx.cuh", "dsa_internal.h"]}
 
 
 def traffic_for(kernel, units):
