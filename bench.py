@@ -743,7 +743,7 @@ def bench_decode(dsa, synth, args, peaks, cid=5):
     scores = torch.empty((cfg.B, ld), dtype=torch.float32, device="cuda")
     idx = torch.empty((cfg.B, cfg.k), dtype=torch.int32, device="cuda")
     out = torch.empty((cfg.B, cfg.H, 512), dtype=torch.bfloat16, device="cuda")
-    n_split = dsa.decode_split(cfg.B)
+    n_split = dsa.decode_split(cfg.B)   # the key split dsa_forward's decode uses
     n_ws = dsa.lib.dsa_sparse_attn_split_workspace_size(cfg.B, cfg.H, n_split)
     split_ws = torch.empty(n_ws, dtype=torch.uint8, device="cuda") if n_ws else None
 

@@ -169,14 +169,21 @@ dsa_status_t dsa_sparse_attn(const uint16_t* q, const uint16_t* kv, int64_t n_kv
                              uint16_t* out, float* lse, int32_t* dev_status, dsa_stream_t stream);
 
 /*
- * dsa_sparse_attn_split — dsa_sparse_attn with each row's selected keys spread over n_split
- * independent partial attentions (a share of the slots each) that a second kernel merges
- * exactly (log-sum-exp weights).  Same inputs, outputs and rules as dsa_sparse_attn; this is how
- * the decode forward fills the GPU when it has few sequences.  `ws` is a caller-owned device
- * buffer of dsa_sparse_attn_split_workspace_size(T, H, n_split) bytes (256-byte aligned) holding
- * the partial outputs; n_split in [1, 8] (1 = dsa_sparse_attn, no workspace needed).
+ * dsa_sparse_attn_split — dsa_sparse_attn with the rows' selected keys spread over partial
+ * attentions that a second kernel merges exactly (log-sum-exp weights).  Same inputs, outputs and
+ * rules as dsa_sparse_attn; this is how the decode forward fills the GPU when it has few sequences.
+ *   n_split in [1, 8]: each row's slots in n_split equal shares; `ws` holds
+ *       dsa_sparse_attn_split_workspace_size(T, H, n_split) bytes (n_split = 1: dsa_sparse_attn,
+ *       no workspace).
+ *   n_split = 0: balanced over every SM pair of the GPU: the rows' ceil(k / 64) tiles of 64 slots,
+ *       end to end, are cut into equal contiguous ranges, one per pair (74 on a B300), so every pair
+ *       gets the same number of tiles whatever T is; `ws` holds
+ *       dsa_sparse_attn_balanced_workspace_size(T, H, k) bytes (0 when no row is split).  This is
+ *       the decode forward's partition.
+ * `ws` is a caller-owned device buffer, 256-byte aligned, holding the partial outputs.
  */
 size_t dsa_sparse_attn_split_workspace_size(int T, int H, int n_split);
+size_t dsa_sparse_attn_balanced_workspace_size(int T, int H, int k);
 dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows,
                                    const int32_t* block_table, int64_t bt_stride, int page_size,
                                    const int32_t* idx, int T, int H, int k, float scale,

@@ -26,7 +26,7 @@ EXPORTS = ("dsa_status_string", "dsa_version", "dsa_index", "dsa_index_paged", "
            "dsa_decode_noalloc", "dsa_decode_noalloc_capacity", "dsa_sparse_attn_split_workspace_size",
            "dsa_sparse_attn_split", "dsa_prefill_host_workspace_size", "dsa_prefill_host",
            "dsa_dense_causal_attn", "dsa_indexer_loss", "dsa_wait_limit_ns", "dsa_forward_loss_workspace_size",
-           "dsa_forward_loss", "dsa_status", "dsa_sparse_attn_backward")
+           "dsa_forward_loss", "dsa_status", "dsa_sparse_attn_backward", "dsa_sparse_attn_balanced_workspace_size")
 
 
 class DSAError(RuntimeError):
@@ -75,6 +75,7 @@ def _load():
         "dsa_decode_noalloc": ([ctypes.POINTER(ForwardArgs), P], I),
         "dsa_decode_noalloc_capacity": ([], ctypes.c_size_t),
         "dsa_sparse_attn_split_workspace_size": ([I, I, I], ctypes.c_size_t),
+        "dsa_sparse_attn_balanced_workspace_size": ([I, I, I], ctypes.c_size_t),
         "dsa_dense_causal_attn": ([P, P, I64, I, I, I64, F, P, P, P, P], I),
         "dsa_wait_limit_ns": ([], ctypes.c_uint64),
         "dsa_indexer_loss": ([P, P, I64, P, I, I, I, I64, F, P, P, I64, P, P, P, P, P], I),
@@ -276,7 +277,8 @@ def decode_split(B: int) -> int:
 
 
 def sparse_attn_split(q, kv, idx, scale, n_split, block_table=None, out=None, lse=None, ws=None, status=None):
-    """dsa_sparse_attn_split: attention with each row's keys spread over n_split partial passes."""
+    """dsa_sparse_attn_split: attention with each row's keys spread over n_split partial passes
+    (n_split = 0: the balanced partition over every SM pair that the decode forward uses)."""
     _need(q, torch.bfloat16, "q", 3)
     _need(kv, torch.bfloat16, "kv")
     _need(idx, torch.int32, "idx", 2)
@@ -284,7 +286,8 @@ def sparse_attn_split(q, kv, idx, scale, n_split, block_table=None, out=None, ls
     page_size = kv.shape[1] if block_table is not None else 0
     if out is None:
         out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
-    n = lib.dsa_sparse_attn_split_workspace_size(T, H, n_split)
+    n = (lib.dsa_sparse_attn_balanced_workspace_size(T, H, idx.shape[1]) if n_split == 0
+         else lib.dsa_sparse_attn_split_workspace_size(T, H, n_split))
     if ws is None and n:
         ws = torch.empty(n, dtype=torch.uint8, device=q.device)
     bt_stride = block_table.stride(0) if block_table is not None else 0

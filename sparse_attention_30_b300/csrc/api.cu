@@ -173,15 +173,36 @@ struct FwdPlan {
   int rows;          // query rows in total
   int chunk;         // rows scored per indexer / top-k launch
   int64_t ld;        // score row pitch (floats)
-  int n_split;       // decode: clusters per sequence in the attention (1 = no key split)
+  int n_split;       // decode: partial results per sequence in the attention (1 = none)
+  int bal_tiles;     // decode: virtual 64-key tiles per sequence of the balanced partition
+  int n_clusters;    // decode: clusters the partition is cut for
   size_t scores_bytes, idx_bytes, part_o_bytes, part_ml_bytes, total;
 };
 
 // Decode attention runs one 2-SM cluster per sequence; with few sequences each one's selected
-// keys are split over several clusters so the 74 cluster slots of the GPU fill up.
+// keys are split over several clusters so that the 74 cluster slots of the GPU fill up.  (The
+// balanced partition below spreads every pair's share evenly, but each extra work item costs a Q
+// load and an fp32 partial epilogue: it measured slower for 32 and 64 sequences, 72.4 vs 68.4 us
+// and 112.7 vs 93.8 us, so the decode forward keeps this split.)
 int decode_split(int B) {
   if (B <= 0 || B >= 74) return 1;
   return std::max(1, std::min(4, 74 / B));
+}
+
+// Balanced partition of the attention (dsa_sparse_attn_split with n_split = 0): the rows' tiles,
+// end to end, cut into equal contiguous ranges, one per 2-SM cluster (74 on a B300); a row spread
+// over several clusters leaves one partial result per cluster.
+struct BalPlan {
+  int tpr, n_clusters, parts;
+};
+BalPlan plan_balanced(int rows, int tiles_per_row) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  BalPlan b{std::max(1, tiles_per_row), 1, 1};
+  const int64_t G = static_cast<int64_t>(rows) * b.tpr;
+  b.n_clusters = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / 2, G)));
+  for (int t = 0; t < rows; ++t) b.parts = std::max(b.parts, bal_parts(t, b.tpr, G, b.n_clusters));
+  return b;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -209,6 +230,8 @@ dsa_status_t plan_forward(const dsa_forward_args* a, FwdPlan* p) {
     return DSA_ERR_INVALID_ARG;
   }
   p->n_split = a->mode == DSA_MODE_DECODE ? decode_split(a->B) : 1;
+  p->bal_tiles = 0;
+  p->n_clusters = 0;
   p->scores_bytes = align256(static_cast<size_t>(p->chunk) * p->ld * sizeof(float));
   p->idx_bytes = a->idx ? 0 : align256(static_cast<size_t>(std::max(1, p->rows)) * a->k * sizeof(int32_t));
   p->part_o_bytes = p->n_split > 1 ? align256(static_cast<size_t>(p->rows) * p->n_split * a->H * 512 * 4) : 0;
@@ -328,7 +351,7 @@ namespace {
 dsa_status_t sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows, const int32_t* block_table,
                                int64_t bt_stride, int page_size, const int32_t* idx, int T, int H, int k, float scale,
                                uint16_t* out, float* lse, int n_split, float* part_o, float* part_ml,
-                               int32_t* dev_status, cudaStream_t stream) {
+                               int32_t* dev_status, cudaStream_t stream, int bal_tiles = 0, int n_clusters = 0) {
   dsa_status_t st = check_attn_args(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, out);
   if (st != DSA_OK || T == 0) return st;
   int* status = status_target(dev_status);
@@ -339,6 +362,7 @@ dsa_status_t sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_t n_
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = out; a.lse = lse; a.status = status; a.limit_ns = wait_limit_ns();
   a.n_split = n_split; a.part_o = part_o; a.part_ml = part_ml;
+  a.bal_tiles = bal_tiles; a.n_clusters = n_clusters;
   return from_cuda(launch_sparse_attn(a, stream));
 }
 }  // namespace
@@ -356,11 +380,30 @@ extern "C" size_t dsa_sparse_attn_split_workspace_size(int T, int H, int n_split
   return split_part_o_bytes(T, H, n_split) + split_part_ml_bytes(T, H, n_split);
 }
 
+extern "C" size_t dsa_sparse_attn_balanced_workspace_size(int T, int H, int k) {
+  if (T < 1 || H < 1 || H > 128 || k < 1 || k > 65536) return 0;
+  const BalPlan b = plan_balanced(T, (k + 63) / 64);
+  if (b.parts == 1) return 0;
+  return split_part_o_bytes(T, H, b.parts) + split_part_ml_bytes(T, H, b.parts);
+}
+
 extern "C" dsa_status_t dsa_sparse_attn_split(const uint16_t* q, const uint16_t* kv, int64_t n_kv_rows,
                                               const int32_t* block_table, int64_t bt_stride, int page_size,
                                               const int32_t* idx, int T, int H, int k, float scale, uint16_t* out,
                                               float* lse, int n_split, void* ws, size_t ws_bytes,
                                               int32_t* dev_status, dsa_stream_t stream) {
+  if (n_split == 0) {  // balanced partition over every SM pair
+    dsa_status_t st = check_attn_args(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, out);
+    if (st != DSA_OK || T == 0) return st;
+    const BalPlan b = plan_balanced(T, (k + 63) / 64);
+    const size_t need = dsa_sparse_attn_balanced_workspace_size(T, H, k);
+    if (need > 0 && (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))) return DSA_ERR_WORKSPACE;
+    char* w = static_cast<char*>(ws);
+    return sparse_attn_split(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, scale, out, lse,
+                             b.parts, b.parts > 1 ? reinterpret_cast<float*>(w) : nullptr,
+                             b.parts > 1 ? reinterpret_cast<float*>(w + split_part_o_bytes(T, H, b.parts)) : nullptr,
+                             dev_status, stream, b.tpr, b.n_clusters);
+  }
   if (n_split < 1 || n_split > 8) return DSA_ERR_INVALID_ARG;
   if (n_split == 1)
     return sparse_attn_split(q, kv, n_kv_rows, block_table, bt_stride, page_size, idx, T, H, k, scale, out, lse, 1,
@@ -480,7 +523,8 @@ dsa_status_t dsa_forward(const dsa_forward_args* a, void* ws, size_t ws_bytes, d
   return sparse_attn_split(a->q, a->kv, a->n_pages * a->page_size, a->block_table, a->bt_stride, a->page_size, idx,
                            a->B, a->H, a->k, a->scale, a->out, a->lse, p.n_split,
                            p.n_split > 1 ? reinterpret_cast<float*>(part) : nullptr,
-                           p.n_split > 1 ? reinterpret_cast<float*>(part + p.part_o_bytes) : nullptr, wst, s);
+                           p.n_split > 1 ? reinterpret_cast<float*>(part + p.part_o_bytes) : nullptr, wst, s,
+                           p.bal_tiles, p.n_clusters);
 }
 
 size_t dsa_forward_loss_workspace_size(const dsa_forward_args* args, int stage) {

@@ -87,6 +87,12 @@ struct AttnArgs {
   int n_split;
   float* part_o;              // [T, n_split, H, 512] fp32, each normalised by its own sum
   float* part_ml;             // [T, n_split, H, 2] fp32: running max (log2 domain) and sum
+  // balanced partition (bal_tiles > 0): the T rows' bal_tiles virtual 64-key tiles each, end to end,
+  // cut into n_clusters equal contiguous ranges (one per cluster); a row spread over several
+  // clusters leaves one partial result per cluster, at part index (cluster - the row's first
+  // cluster) < n_split, and launch_attn_combine merges them
+  int bal_tiles;
+  int n_clusters;
   // indexer-loss mode (lse_in non-NULL): no attention output; the head-summed attention target
   // over each row's set and its KL divergence from the softmax of the indexer scores
   const float* lse_in;        // [T, H] natural-log normalisers of the forward over the same sets
@@ -97,6 +103,18 @@ struct AttnArgs {
   double* loss_acc;           // sum over rows added here, or NULL
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+
+// Balanced partition of G = rows x tiles-per-row virtual tiles over n_cl clusters: cluster c covers
+// [bal_bound(c), bal_bound(c + 1)); bal_cluster(g) is the cluster whose range holds tile g (n_cl <= G).
+__host__ __device__ inline int64_t bal_bound(int64_t c, int64_t G, int n_cl) { return c * G / n_cl; }
+__host__ __device__ inline int bal_cluster(int64_t g, int64_t G, int n_cl) {
+  return static_cast<int>(((g + 1) * n_cl - 1) / G);
+}
+// Number of clusters (partial results) row t is spread over.
+__host__ __device__ inline int bal_parts(int t, int tpr, int64_t G, int n_cl) {
+  const int64_t g0 = static_cast<int64_t>(t) * tpr;
+  return bal_cluster(g0 + tpr - 1, G, n_cl) - bal_cluster(g0, G, n_cl) + 1;
+}
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- sparse attention backward

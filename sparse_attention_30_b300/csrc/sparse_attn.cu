@@ -94,10 +94,10 @@ __device__ __forceinline__ int64_t latent_row(const AttnArgs& a, int t, int32_t 
   return r;
 }
 
-// A work item: tiles [tile0, tile0 + n_tiles) of token t's selection, written as key-split share
-// sp (t < 0: no more items).
+// A work item: tiles [tile0, tile0 + n_tiles) of token t's selection, written as partial result
+// sp (t < 0: no more items); nt is the token of this cluster's next item (-1: none).
 struct Item {
-  int t, sp, tile0, n_tiles;
+  int t, sp, tile0, n_tiles, nt;
 };
 
 struct Bars {
@@ -135,6 +135,7 @@ __device__ __forceinline__ bool read_item(Bars& bars, const Item* sched, int j, 
   it->sp = e->sp;
   it->tile0 = e->tile0;
   it->n_tiles = e->n_tiles;
+  it->nt = e->nt;
   __syncwarp();
   if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(baddr(bars.sched_empty[slot]));
   return true;
@@ -497,16 +498,37 @@ __device__ __forceinline__ void attn_body(const AttnArgs& a, const CUtensorMap* 
       if (!__all_sync(0xffffffffu, ptx::mbar_wait_sleep(baddr(bars.sched_empty[slot]), ((j / kSched) & 1) ^ 1,
                                                         abort_flag, a.status, a.limit_ns, 1000)))
         break;
-      const int id = cl + j * n_cl;
-      Item it{-1, 0, 0, 0};
-      if (id < n_items) {
-        it.t = id / a.n_split;
-        it.sp = id % a.n_split;
-        const int64_t n_keys = dense ? a.q_pos0 + it.t + 1 : first_empty_slot(a.idx + static_cast<int64_t>(it.t) * a.k, a.k);
-        const int all_tiles = static_cast<int>((n_keys + kKT - 1) / kKT);
-        const int per = (all_tiles + a.n_split - 1) / a.n_split;
-        it.tile0 = it.sp * per;
-        it.n_tiles = max(0, min(per, all_tiles - it.sp * per));
+      Item it{-1, 0, 0, 0, -1};
+      if (a.bal_tiles > 0) {
+        // balanced: this cluster's contiguous range of the rows' virtual tiles, row by row
+        const int tpr = a.bal_tiles;
+        const int64_t G = static_cast<int64_t>(a.T) * tpr;
+        const int64_t lo = bal_bound(cl, G, n_cl), hi = bal_bound(cl + 1, G, n_cl);
+        const int t = static_cast<int>(lo / tpr) + j;
+        const int64_t g0 = static_cast<int64_t>(t) * tpr;
+        if (lo < hi && g0 < hi) {
+          it.t = t;
+          it.sp = cl - bal_cluster(g0, G, n_cl);
+          const int v0 = static_cast<int>((lo > g0 ? lo : g0) - g0);
+          const int v1 = static_cast<int>((hi < g0 + tpr ? hi : g0 + tpr) - g0);
+          const int real = (first_empty_slot(a.idx + static_cast<int64_t>(t) * a.k, a.k) + kKT - 1) / kKT;
+          it.tile0 = v0;
+          it.n_tiles = max(0, min(v1, real) - v0);
+          it.nt = g0 + tpr < hi ? t + 1 : -1;
+        }
+      } else {
+        const int id = cl + j * n_cl;
+        if (id < n_items) {
+          it.t = id / a.n_split;
+          it.sp = id % a.n_split;
+          const int64_t n_keys = dense ? a.q_pos0 + it.t + 1 : first_empty_slot(a.idx + static_cast<int64_t>(it.t) * a.k, a.k);
+          const int all_tiles = static_cast<int>((n_keys + kKT - 1) / kKT);
+          const int per = (all_tiles + a.n_split - 1) / a.n_split;
+          it.tile0 = it.sp * per;
+          it.n_tiles = max(0, min(per, all_tiles - it.sp * per));
+          const int next_id = id + n_cl;
+          it.nt = next_id < n_items ? next_id / a.n_split : -1;
+        }
       }
       if (lane == 0) {
         volatile Item* e = sched + slot;
@@ -514,6 +536,7 @@ __device__ __forceinline__ void attn_body(const AttnArgs& a, const CUtensorMap* 
         e->sp = it.sp;
         e->tile0 = it.tile0;
         e->n_tiles = it.n_tiles;
+        e->nt = it.nt;
         ptx::mbar_arrive(baddr(bars.sched_full[slot]));
       }
       if (it.t < 0) break;
@@ -540,13 +563,10 @@ __device__ __forceinline__ void attn_body(const AttnArgs& a, const CUtensorMap* 
           for (int b = 0; b < 9; ++b)
             ptx::tma_load_2d_hint(sbase + kOffK + b * kQBoxBytes, qmap, baddr(bars.q_full), b * 64, it.t * a.H,
                                   ptx::l2_evict_first_policy());  // Q and O stream: keep L2 for latent rows
-          // the next item's Q (work items are dealt round-robin) into L2, so that its load after this
-          // item's last product is an L2 hit
-          const int64_t next_id = cl + static_cast<int64_t>(j + 1) * n_cl;
-          if (next_id < static_cast<int64_t>(a.T) * a.n_split) {
-            const int nt = static_cast<int>(next_id / a.n_split);
+          // the next item's Q into L2, so that its load after this item's last product is an L2 hit
+          if (it.nt >= 0 && it.nt != it.t) {
 #pragma unroll 1
-            for (int b = 0; b < 9; ++b) ptx::tma_prefetch_2d(qmap, b * 64, nt * a.H);
+            for (int b = 0; b < 9; ++b) ptx::tma_prefetch_2d(qmap, b * 64, it.nt * a.H);
           }
         }
         __syncwarp();
@@ -986,38 +1006,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   attn_body<kMode | 2>(a, &qmap, &kvmap);
 }
 
-// Merges the key-split partial results of one (token, head) row: with per-split running max m_s
-// (log2 domain), sum l_s and normalised output O_s, the row's softmax weights over the union of the
-// splits give O = sum_s l_s 2^(m_s - m) O_s / sum_s l_s 2^(m_s - m), m = max_s m_s.
+// Merges the partial results of one (token, head) row: with per-part running max m_s (log2 domain),
+// sum l_s and normalised output O_s, the row's softmax weights over the union of the parts give
+// O = sum_s l_s 2^(m_s - m) O_s / sum_s l_s 2^(m_s - m), m = max_s m_s.  The parts of a row are
+// n_split (key split), or, in the balanced partition, the clusters its tiles were spread over.
 __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
-  constexpr int kMaxSplit = 8;
   const int t = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int np = a.bal_tiles > 0
+                     ? bal_parts(t, a.bal_tiles, static_cast<int64_t>(a.T) * a.bal_tiles, a.n_clusters)
+                     : a.n_split;
   const int64_t base = static_cast<int64_t>(t) * a.n_split * a.H + h;
-  // every load is issued before any is used (one memory round trip, not two)
-  float ms[kMaxSplit], ls[kMaxSplit];
-  float4 o[kMaxSplit];
-#pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) {
-    if (s < a.n_split) {
-      const int64_t r = base + static_cast<int64_t>(s) * a.H;
-      const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[r];
-      ms[s] = ml.x;
-      ls[s] = ml.y;
-      o[s] = reinterpret_cast<const float4*>(a.part_o + r * kDV)[threadIdx.x];
-    }
-  }
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
   float m = -INFINITY;
-#pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s)
-    if (s < a.n_split) m = fmaxf(m, ms[s]);
+  for (int s = 0; s < np; ++s) m = fmaxf(m, ml[base + static_cast<int64_t>(s) * a.H].x);
   float wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // loads of a few parts are issued before they are used (one memory round trip per group)
+  for (int s0 = 0; s0 < np; s0 += 4) {
+    float4 o[4];
+    float2 p[4];
 #pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) {
-    if (s < a.n_split) {
-      const float wt = (ls[s] > 0.f && m > -INFINITY) ? ls[s] * fast_exp2(ms[s] - m) : 0.f;
-      acc.x += wt * o[s].x; acc.y += wt * o[s].y; acc.z += wt * o[s].z; acc.w += wt * o[s].w;
-      wsum += wt;
+    for (int u = 0; u < 4; ++u) {
+      if (s0 + u < np) {
+        const int64_t r = base + static_cast<int64_t>(s0 + u) * a.H;
+        p[u] = ml[r];
+        o[u] = reinterpret_cast<const float4*>(a.part_o + r * kDV)[threadIdx.x];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (s0 + u < np) {
+        const float wt = (p[u].y > 0.f && m > -INFINITY) ? p[u].y * fast_exp2(p[u].x - m) : 0.f;
+        acc.x += wt * o[u].x; acc.y += wt * o[u].y; acc.z += wt * o[u].z; acc.w += wt * o[u].w;
+        wsum += wt;
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -1059,6 +1081,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a0, cudaStream_t stream) {
   AttnArgs a = a0;
   const bool loss = a.lse_in != nullptr;
   if (loss || a.n_split < 1 || a.part_o == nullptr || a.part_ml == nullptr) a.n_split = 1;
+  if (loss || a.idx == nullptr || a.n_clusters < 1) a.bal_tiles = 0;  // (the host splits no row without buffers)
   // Q viewed as [T*H, 576] bf16, box 64 x 128 (rows past the tensor read as zero)
   CUtensorMap qmap;
   const uint64_t rows = static_cast<uint64_t>(a.T) * a.H;
@@ -1080,8 +1103,9 @@ cudaError_t launch_sparse_attn(const AttnArgs& a0, cudaStream_t stream) {
     e = dense ? launch_mode<3>(a, qmap, kvmap, ctas, stream) : launch_mode<2>(a, qmap, kvmap, ctas, stream);
     return e;
   }
-  // one cluster per SM pair, each taking every n_clusters-th work item
-  const int clusters = static_cast<int>(items < sms / 2 ? items : sms / 2);
+  // one cluster per SM pair, each taking every n_clusters-th work item (balanced: the clusters the
+  // partition was cut for)
+  const int clusters = a.bal_tiles > 0 ? a.n_clusters : static_cast<int>(items < sms / 2 ? items : sms / 2);
   e = dense ? launch_mode<1>(a, qmap, kvmap, 2 * clusters, stream) : launch_mode<0>(a, qmap, kvmap, 2 * clusters, stream);
   if (e != cudaSuccess || a.n_split == 1) return e;
   return launch_attn_combine(a, stream);

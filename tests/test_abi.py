@@ -237,22 +237,50 @@ def test_product_path_does_not_import_the_oracle():
                 assert "oracle/" not in text, fn
 
 
+def _bal_parts(rows, tpr, n_cl):
+    """Most clusters any row is spread over when rows x tpr tiles are cut into n_cl equal ranges
+    (cluster c covers tiles [c G / n_cl, (c + 1) G / n_cl))."""
+    G = rows * tpr
+    cl = lambda g: ((g + 1) * n_cl - 1) // G
+    return max(cl(t * tpr + tpr - 1) - cl(t * tpr) + 1 for t in range(rows))
+
+
 def test_decode_split_mirror_matches_library_workspace():
     # the binding's decode_split mirrors the library's key-split choice; the library's decode
     # workspace holds the fp32 partial outputs exactly when it splits, so the sizes must agree
     dsa = _lib()
     H, k, max_len = 128, 2048, 4096
+    r256 = lambda x: (x + 255) // 256 * 256
     for B in [1, 2, 5, 18, 19, 36, 37, 73, 74, 75, 200]:
         d = dsa.ForwardArgs(mode=dsa.MODE_DECODE, H_I=64, H=H, k=k, scale=0.07, B=B, page_size=64,
                             n_pages=B * 64, bt_stride=64, max_seq_len=max_len)
         n = dsa.lib.dsa_forward_workspace_size(ctypes.byref(d))
-        r256 = lambda x: (x + 255) // 256 * 256
         split = dsa.decode_split(B)
         want = 256 + r256(B * max_len * 4) + r256(B * k * 4)
         if split > 1:
             want += r256(B * split * H * 512 * 4) + r256(B * split * H * 2 * 4)
         assert n == want, (B, split, n, want)
         assert split == (1 if B >= 74 else max(1, min(4, 74 // B)))
+
+
+def test_balanced_partition_workspace():
+    # dsa_sparse_attn_split with n_split = 0 cuts the rows' ceil(k / 64) tiles each, end to end, into
+    # equal contiguous ranges, one per SM pair (74 here: with no GPU the library assumes a B300's
+    # 148 SMs); its workspace holds one fp32 partial result per cluster a row is spread over
+    dsa = _lib()
+    H, k = 128, 2048
+    r256 = lambda x: (x + 255) // 256 * 256
+    for B in [1, 2, 5, 18, 32, 37, 64, 74, 75, 148, 200]:
+        tpr = k // 64
+        n_cl = min(74, B * tpr)
+        parts = _bal_parts(B, tpr, n_cl)
+        bal = dsa.lib.dsa_sparse_attn_balanced_workspace_size(B, H, k)
+        assert bal == (0 if parts == 1 else r256(B * parts * H * 512 * 4) + r256(B * parts * H * 2 * 4)), B
+        G = B * tpr
+        sizes = [(c + 1) * G // n_cl - c * G // n_cl for c in range(n_cl)]
+        assert max(sizes) - min(sizes) <= 1 and sum(sizes) == G          # equal shares, within one tile
+    assert _bal_parts(64, 32, 74) == 3 and _bal_parts(1, 32, 32) == 32
+    assert dsa.lib.dsa_sparse_attn_balanced_workspace_size(0, H, k) == 0
 
 
 def test_default_prefill_chunk_keeps_the_score_block_near_one_gib():

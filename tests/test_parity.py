@@ -452,7 +452,7 @@ def test_forward_loss_matches_the_separate_calls(dsa, stage):
     assert abs(loss - kl_ref.double().sum().item()) <= 1e-5 * max(1.0, abs(loss))
 
 
-@pytest.mark.parametrize("n_split", [2, 3, 8])
+@pytest.mark.parametrize("n_split", [0, 2, 3, 8])   # 0: the balanced partition (here up to 13 parts per row)
 def test_attention_key_split_matches_oracle(dsa, n_split):
     g = torch.Generator().manual_seed(21 + n_split)
     T, H, S, k = 6, 128, 5000, 2048
