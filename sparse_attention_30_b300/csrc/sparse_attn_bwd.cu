@@ -25,6 +25,9 @@
 //     written into its own and rank 0's shared memory; dq[:, 0:320] += dS V[:, 0:320];
 //     dv^T = dO^T P for four 128-dim blocks into dkv[:, 0:512].
 //
+// In each CTA one warp issues S (or dP) and the dq products and a second warp issues the dc^T (or
+// dv^T) products, so that the two chains of tensor-core instructions are issued side by side.
+//
 // Persistent: one cluster per SM pair takes every (number of clusters)-th token.  Every wait is
 // bounded (the kernel records DSA_ERR_DEVICE_TIMEOUT and leaves); an out-of-range position is
 // skipped and reported as DSA_ERR_DEVICE_RANGE.
@@ -45,7 +48,8 @@ constexpr int kProducers = kProdWarps * 32;
 constexpr int kRowWarp0 = 1 + kProdWarps;      // warps 9..12: one head row per thread
 constexpr int kEpiWarp0 = kRowWarp0 + 4;       // warps 13..16: dc blocks and dq read-out
 constexpr int kCreditWarp = kEpiWarp0 + 4;     // warp 17: Q / dO loads and slot credits
-constexpr int kThreads = 32 * (kCreditWarp + 1);
+constexpr int kDcWarp = kCreditWarp + 1;       // warp 18: issues the dc^T / dv^T products
+constexpr int kThreads = 32 * (kDcWarp + 1);
 constexpr int kDL = 576, kDV = 512;
 constexpr int kBox = 128 * 128;                // [128 rows x 64 dims] bf16, 128B-swizzled (TMA box)
 constexpr int kBlk = kKT * 128;                // [32 rows x 64 dims] bf16, 128B-swizzled
@@ -189,9 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(baddr(bars.p_empty[b]), 1);
       }
       ptx::mbar_init(baddr(bars.q_full), 1);
-      ptx::mbar_init(baddr(bars.q_free), 1);
+      ptx::mbar_init(baddr(bars.q_free), 2);         // both MMA warps read Q
       ptx::mbar_init(baddr(bars.ds_full), 1);
-      ptx::mbar_init(baddr(bars.ds_consumed), 1);
+      ptx::mbar_init(baddr(bars.ds_consumed), 2);    // the dq product and the dc^T products
       ptx::mbar_arrive_expect_tx(baddr(bars.ds_full), kSlot);  // armed for the first copy
     } else {
       for (int s = 0; s < kStages; ++s) {
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(baddr(bars.dsl_empty[b]), 1);
       }
       ptx::mbar_init(baddr(bars.do_full), 1);
-      ptx::mbar_init(baddr(bars.do_free), 1);
+      ptx::mbar_init(baddr(bars.do_free), 2);        // both MMA warps read dO
       ptx::mbar_init(baddr(bars.ds_peer_empty), 1);
     }
     for (int j = 0; j < kNDc0; ++j) {
@@ -216,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(baddr(bars.dq_full), 1);
     ptx::mbar_init(baddr(bars.dq_free), 128);
-    ptx::mbar_init(baddr(bars.mma_done), 1);
+    ptx::mbar_init(baddr(bars.mma_done), 2);
     abort_flag_s = 0;
     ptx::fence_mbar_init();
   }
@@ -238,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (rank == 0) {
       constexpr uint32_t kIdS = ptx::instr_desc(128, kKT, 1, 1, 0, 0);
       constexpr uint32_t kIdDq = ptx::instr_desc(128, 256, 1, 1, 0, 1);
-      constexpr uint32_t kIdDc = ptx::instr_desc(128, kKT, 1, 1, 1, 1);
       const uint32_t q_s = sbase + kOffQ, ds_s = sbase + kOffDs0;
       for (int t = cl; ok && t < a.T; t += n_cl) {
         const int n = tiles_of(a, t);
@@ -282,20 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_bf16_warp(tmem + kColDq0, desc_sw64(ds_s + ks * 32), desc_sw128_mn(kst + 5 * kBlk + ks * 16 * 128, kBlk),
                                kIdDq, (i > 0 || ks > 0) ? 1u : 0u);
           ptx::mma_commit_warp(baddr(bars.k_empty[st]));
-          // dc^T block j [dims 128j.., 32 keys] = Q^T dS
-          for (int j = 0; j < kNDc0 && ok; ++j) {
-            if (!warp_wait(baddr(bars.dc_empty[j]), (gi & 1) ^ 1, abort_flag, a)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              ptx::mma_bf16_warp(tmem + kColDc0 + j * kKT, desc_sw128_mn(q_s + 2 * j * kBox + ks * 16 * 128, kBox),
-                                 desc_sw64_mn(ds_s + ks * 16 * 64), kIdDc, ks > 0 ? 1u : 0u);
-            ptx::mma_commit_warp(baddr(bars.dc_full[j]));
-          }
-          ptx::mma_commit_warp(baddr(bars.ds_consumed));
+          ptx::mma_commit_warp(baddr(bars.ds_consumed));  // (the dc^T products are the other warp's)
         }
         if (!ok) break;
         ptx::mma_commit_warp(baddr(bars.dq_full));
@@ -307,7 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdDp = ptx::instr_desc(128, kKT, 1, 1, 0, 0);
       constexpr uint32_t kIdDq256 = ptx::instr_desc(128, 256, 1, 1, 0, 1);
       constexpr uint32_t kIdDq64 = ptx::instr_desc(128, 64, 1, 1, 0, 1);
-      constexpr uint32_t kIdDc = ptx::instr_desc(128, kKT, 1, 1, 1, 1);
       const uint32_t do_s = sbase + kOffDO;
       for (int t = cl; ok && t < a.T; t += n_cl) {
         const int n = tiles_of(a, t);
@@ -346,7 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_after();
           const uint32_t vst = sbase + kOffV + st * kVStage, dsl = sbase + kOffDs1 + ps * kSlot;
-          const uint32_t p_s = sbase + kOffP + ps * kSlot;
           // dq[:, 0:320] += dS V(i)[:, 0:320]  (blocks 0..3 as one N = 256 product, block 4 as N = 64)
 #pragma unroll
           for (int ks = 0; ks < kKT / 16; ++ks) {
@@ -356,21 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                desc_sw128_mn(vst + 4 * kBlk + ks * 16 * 128, kBlk), kIdDq64, (i > 0 || ks > 0) ? 1u : 0u);
           }
           ptx::mma_commit_warp(baddr(bars.v_empty[st]));
-          ptx::mma_commit_warp(baddr(bars.dsl_empty[ps]));
-          // dv^T block j [dims 128j.., 32 keys] = dO^T P
-          for (int j = 0; j < kNDc1 && ok; ++j) {
-            if (!warp_wait(baddr(bars.dc_empty[j]), (gi & 1) ^ 1, abort_flag, a)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              ptx::mma_bf16_warp(tmem + kColDc1 + j * kKT, desc_sw128_mn(do_s + 2 * j * kBox + ks * 16 * 128, kBox),
-                                 desc_sw64_mn(p_s + ks * 16 * 64), kIdDc, ks > 0 ? 1u : 0u);
-            ptx::mma_commit_warp(baddr(bars.dc_full[j]));
-          }
-          ptx::mma_commit_warp(baddr(bars.p_consumed[ps]));
+          ptx::mma_commit_warp(baddr(bars.dsl_empty[ps]));  // (the dv^T products are the other warp's)
         }
         if (!ok) break;
         ptx::mma_commit_warp(baddr(bars.dq_full));
@@ -378,6 +352,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         g += n;
         ++nq;
       }
+    }
+    ptx::mma_commit_warp(baddr(bars.mma_done));
+    drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
+  } else if (warp == kDcWarp) {
+    // ================================================================ second MMA warp: the latent-row
+    // gradient products, issued beside the S / dP and dq products of warp 0
+    constexpr uint32_t kIdDc = ptx::instr_desc(128, kKT, 1, 1, 1, 1);
+    int g = 0, nq = 0;
+    bool ok = true;
+    for (int t = cl; ok && t < a.T; t += n_cl) {
+      const int n = tiles_of(a, t);
+      if (n == 0) continue;
+      if (!warp_wait(rank == 0 ? baddr(bars.q_full) : baddr(bars.do_full), nq & 1, abort_flag, a)) break;
+      ptx::tc_fence_after();
+      for (int i = 0; i < n; ++i) {
+        const int gi = g + i, ps = gi & 1;
+        // rank 0: dS(i) in this CTA's slot; rank 1: dS(i) in the local slot, written after P(i) arrived
+        const bool got = rank == 0 ? warp_wait_cluster(baddr(bars.ds_full), gi & 1, abort_flag, a)
+                                   : warp_wait(baddr(bars.dsl_full[ps]), (gi >> 1) & 1, abort_flag, a);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_after();
+        const int nblk = rank == 0 ? kNDc0 : kNDc1;
+        const uint32_t col = rank == 0 ? kColDc0 : kColDc1;
+        const uint32_t lhs = sbase + (rank == 0 ? kOffQ : kOffDO);            // Q^T or dO^T, MN-major
+        const uint32_t rhs = sbase + (rank == 0 ? kOffDs0 : kOffP + ps * kSlot);  // dS or P, MN-major
+        for (int j = 0; j < nblk && ok; ++j) {
+          // block j [dims 128j.., 32 keys]
+          if (!warp_wait(baddr(bars.dc_empty[j]), (gi & 1) ^ 1, abort_flag, a)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            ptx::mma_bf16_warp(tmem + col + j * kKT, desc_sw128_mn(lhs + 2 * j * kBox + ks * 16 * 128, kBox),
+                               desc_sw64_mn(rhs + ks * 16 * 64), kIdDc, ks > 0 ? 1u : 0u);
+          ptx::mma_commit_warp(baddr(bars.dc_full[j]));
+        }
+        if (!ok) break;
+        ptx::mma_commit_warp(rank == 0 ? baddr(bars.ds_consumed) : baddr(bars.p_consumed[ps]));
+      }
+      if (!ok) break;
+      ptx::mma_commit_warp(rank == 0 ? baddr(bars.q_free) : baddr(bars.do_free));
+      g += n;
+      ++nq;
     }
     ptx::mma_commit_warp(baddr(bars.mma_done));
     drain_wait(baddr(bars.mma_done), 0, a.limit_ns);
