@@ -419,6 +419,9 @@ def run_ours(args, dist, rank, ws):
         line["e2e"] = bench_e2e(dsa, d, cfg, args, dist, ws)
     del d, runner, fwd
     torch.cuda.empty_cache()
+    if not args.no_backward:
+        # the training-side companion: the attention backward over the same 128K selections
+        line["backward_128k"] = bench_backward(dsa, synth, args, peaks, L=cfg.L)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_seconds)
     return line
@@ -937,6 +940,7 @@ def main():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-fp8-peak", action="store_true", help="skip the e4m3 GEMM that measures the FP8 peak")
+    p.add_argument("--no-backward", action="store_true", help="skip the 128K attention backward sub-line")
     p.add_argument("--shard", default="sequences", choices=["sequences", "rows"],
                    help="N > 1: one 128K sequence per rank (weak scaling), or one sequence split by query rows "
                         "over the ranks (strong scaling)")
