@@ -420,6 +420,8 @@ __device__ __forceinline__ void loss_row_warps(const AttnArgs& a, Bars& bars, co
 // kMode bit 0: dense causal (no selection; row t attends latent rows 0 .. q_pos0 + t).
 // kMode bit 1: indexer loss (no value pass; every CTA is an independent score CTA, launched without
 // clusters).  Attention modes run as clusters of two.
+// kMode bit 2: the balanced partition of AttnArgs::bal_tiles (a kernel instance of its own, so that
+// the other modes carry none of its scheduling code).
 template <int kMode>
 __device__ __forceinline__ void attn_body(const AttnArgs& a, const CUtensorMap* qmap, const CUtensorMap* kvmap) {
   extern __shared__ uint8_t smem_raw[];
@@ -430,7 +432,7 @@ __device__ __forceinline__ void attn_body(const AttnArgs& a, const CUtensorMap* 
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag_s;
 
-  constexpr bool kDense = (kMode & 1) != 0, kLoss = (kMode & 2) != 0;
+  constexpr bool kDense = (kMode & 1) != 0, kLoss = (kMode & 2) != 0, kBal = (kMode & 4) != 0;
   const int rank = kLoss ? 0 : static_cast<int>(ptx::cluster_ctarank());
   const int cl = kLoss ? blockIdx.x : blockIdx.x >> 1, n_cl = kLoss ? gridDim.x : gridDim.x >> 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -499,7 +501,7 @@ __device__ __forceinline__ void attn_body(const AttnArgs& a, const CUtensorMap* 
                                                         abort_flag, a.status, a.limit_ns, 1000)))
         break;
       Item it{-1, 0, 0, 0, -1};
-      if (a.bal_tiles > 0) {
+      if constexpr (kBal) {
         // balanced: this cluster's contiguous range of the rows' virtual tiles, row by row
         const int tpr = a.bal_tiles;
         const int64_t G = static_cast<int64_t>(a.T) * tpr;
@@ -1057,7 +1059,7 @@ namespace {
 template <int kMode>
 cudaError_t launch_mode(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kvmap, int ctas,
                         cudaStream_t stream) {
-  auto kernel = (kMode & 2) ? indexer_loss_kernel<kMode & 1> : sparse_attn_kernel<kMode & 1>;
+  auto kernel = (kMode & 2) ? indexer_loss_kernel<kMode & 1> : sparse_attn_kernel<kMode & 5>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -1106,7 +1108,9 @@ cudaError_t launch_sparse_attn(const AttnArgs& a0, cudaStream_t stream) {
   // one cluster per SM pair, each taking every n_clusters-th work item (balanced: the clusters the
   // partition was cut for)
   const int clusters = a.bal_tiles > 0 ? a.n_clusters : static_cast<int>(items < sms / 2 ? items : sms / 2);
-  e = dense ? launch_mode<1>(a, qmap, kvmap, 2 * clusters, stream) : launch_mode<0>(a, qmap, kvmap, 2 * clusters, stream);
+  e = dense ? launch_mode<1>(a, qmap, kvmap, 2 * clusters, stream)
+            : a.bal_tiles > 0 ? launch_mode<4>(a, qmap, kvmap, 2 * clusters, stream)
+                              : launch_mode<0>(a, qmap, kvmap, 2 * clusters, stream);
   if (e != cudaSuccess || a.n_split == 1) return e;
   return launch_attn_combine(a, stream);
 }
