@@ -90,14 +90,15 @@ def measure_fp8_peak(n=8192, sustain_s=2.0):
 # from a capture of a given build of that kernel's source.  A figure is reported only while the
 # source still hashes to the captured build; otherwise `traffic` is null.
 TRAFFIC_CAPTURES = {
-    # dram__bytes.sum of one launch over the last 1024 query rows of the 128K prefill (each row against
-    # ~131K keys), per query row; the capture replays from a flushed L2, so it overstates the steady state
-    "sparse_attn": {"src": "f52ab0886cd0fae0", "bytes_per_unit": 612.1e6 / 1024,
-                    "capture": "ncu dram__bytes.sum, sparse_attn_kernel<0> over the 1024-row 128K tail, per row x rows"},
-    "indexer": {"src": "5a7e056d47d32a72", "bytes_per_unit": 539.5e6 / 1024,
-                "capture": "ncu dram__bytes.sum, indexer_kernel<64> over the 1024-row 128K tail, per row x rows"},
-    "topk": {"src": "5cbb3de9049894a9", "bytes_per_unit": 624.6e6 / 1024,
-             "capture": "ncu dram__bytes.sum, topk_kernel over the 1024-row 128K tail, per row x rows"},
+    # dram__bytes_read.sum + dram__bytes_write.sum of one launch over the last 1024 query rows of the 128K
+    # prefill (each row against ~131K keys), per query row; the capture replays from a flushed L2, so
+    # it overstates the steady state a little
+    "sparse_attn": {"src": "de17a35c046c29e4", "bytes_per_unit": (492.850e6 + 117.252e6) / 1024,
+                    "capture": "ncu dram read + write, sparse_attn_kernel<0> over the 1024-row 128K tail, per row x rows"},
+    "indexer": {"src": "14cdd723e1ccffab", "bytes_per_unit": (63.560e6 + 475.289e6) / 1024,
+                "capture": "ncu dram read + write, indexer_kernel<64> over the 1024-row 128K tail, per row x rows"},
+    "topk": {"src": "c8b05f44c8d040ca", "bytes_per_unit": (617.257e6 + 7.713e6) / 1024,
+             "capture": "ncu dram read + write, topk_kernel over the 1024-row 128K tail, per row x rows"},
 }
 
 
