@@ -505,6 +505,24 @@ def test_forward_prefill_config2_sampled_rows(dsa):
     assert swaps <= len(rows)  # near-tie swaps are rare
 
 
+def test_forward_prefill_chunked_selection_matches_the_separate_calls(dsa):
+    """A prefill of eight chunks through dsa_forward selects, for every row, the set that the separate
+    calls (dsa_index, then dsa_topk, chunk by chunk) select: the same scores and the same exact
+    selection, whatever the chunking."""
+    cfg = synth.config(2)
+    d = _cuda(synth.prefill_inputs(cfg))
+    chunk = 512
+    f = _run_prefill(dsa, d, cfg, chunk_rows=chunk)
+    ld = (cfg.L + 3) // 4 * 4
+    scores = torch.empty((chunk, ld), dtype=torch.float32, device="cuda")
+    for r0 in range(0, cfg.L, chunk):
+        rows = slice(r0, r0 + chunk)
+        dsa.index(d["q8"][rows], d["q_scale"][rows], d["w"][rows], d["k8"], d["k_scale"], q_pos0=r0, scores=scores)
+        idx = dsa.topk(scores, cfg.k, q_pos0=r0, n_cols=cfg.L)
+        assert torch.equal(torch.sort(idx, dim=1).values, torch.sort(f.idx[rows], dim=1).values), r0
+    assert dsa.device_status() == 0
+
+
 def test_prefill_host_matches_device_forward(dsa):
     # the host-buffer pipeline (ragged 1000-row chunks through two device slots) gives the device
     # forward's outputs: the same selected sets (the order of a selection is not fixed, and the
