@@ -10,7 +10,8 @@
 // Warp roles (320 threads):
 //   warp 0      TMA producer: the query tile once, then key tiles through a ring of stages
 //   warp 1      owns TMEM and issues the FP8 MMAs (K = 128 as 4 x K32), one elected lane
-//   warps 2..9  two epilogue groups of 4 warps; group g drains TMEM buffer g (tiles i = g mod 2):
+//   warps 2..9  epilogue: every tile's TMEM buffer is drained by all eight, warps w and w + 4
+//               splitting the columns of lanes [32*(w mod 4), +32); head weights in registers;
 //               ReLU, weight, sum over heads, key scale, causal mask, store fp32 scores.
 #include "dsa_internal.h"
 #include "dsa_ptx.cuh"
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(t_full(b), 1);
-      ptx::mbar_init(t_empty(b), 4);
+      ptx::mbar_init(t_empty(b), 8);  // every epilogue warp drains every buffer
     }
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -178,62 +179,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     drain_wait(mma_done, 0, a.limit_ns);
   } else {
     // ------------------------------------------------ epilogue
-    const int g = (warp - 2) >> 2;  // tiles i = g mod 2 use TMEM buffer g
-    const int sub = warp & 3;       // this warp may touch TMEM lanes [32*sub, 32*sub + 32)
+    // Warps w and w + 4 share TMEM lanes [32*sub, 32*sub + 32) (sub = w mod 4) and split the
+    // columns: half h takes the (token, head) columns [128h, 128h + 128) of every tile, so each
+    // thread keeps the 128 head weights of its columns in registers for the whole block.  Read
+    // from shared memory for every tile instead (1 KB per thread per tile), the weights kept the
+    // L1 data pipe 82% busy and set the kernel's time.  TMEM is read 16 columns at a time so that
+    // the weights, the columns and the sums fit in the 168 registers a thread has.
+    constexpr int HALF = C::NCOL / 2;
+    constexpr int TH = C::TT / 2;  // tokens per half
+    const int h = (warp - 2) >> 2;
+    const int sub = warp & 3;
     const int row = sub * 32 + lane;
-    // This group handles tiles g, g+2, g+4, ...; the key scale of a tile is loaded one tile (of the
-    // group) ahead so its latency does not land on the tile being finished.
+    float wr[HALF];
+#pragma unroll
+    for (int c = 0; c < HALF; ++c) wr[c] = sW[h * HALF + c];
+    // the key scale of a tile is loaded one tile ahead so its latency does not land on the tile
+    // being finished
     auto key_of = [&](int i) { return (tb + i) * kTileKeys + row; };
     auto scale_of = [&](int i) -> float {  // 0 for a key past the range
       const int s = key_of(i);
       return (i < n_tiles && s < key_end) ? a.k_scale[s] : 0.f;
     };
-    float sk_next = scale_of(g);
-    for (int i = g; i < n_tiles; i += 2) {
+    float sk_next = scale_of(0);
+    for (int i = 0; i < n_tiles; ++i) {
       const float sk = sk_next;
-      sk_next = scale_of(i + 2);
-      const bool kvalid = key_of(i) < key_end;
+      sk_next = scale_of(i + 1);
       const int s = key_of(i);
+      const bool kvalid = s < key_end;
+      const int buf = i & 1;
       const uint32_t bph = (i >> 1) & 1;
-      if (!ptx::mbar_wait(t_full(g), bph, abort_flag, a.status, a.limit_ns)) break;
+      if (!ptx::mbar_wait(t_full(buf), bph, abort_flag, a.status, a.limit_ns)) break;
       ptx::tc_fence_after();
-      float acc[C::TT][C::NACC];
+      float acc[TH][C::NACC];
 #pragma unroll
-      for (int tt = 0; tt < C::TT; ++tt)
+      for (int tt = 0; tt < TH; ++tt)
 #pragma unroll
         for (int e = 0; e < C::NACC; ++e) acc[tt][e] = 0.f;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(sub * 32) << 16) + g * C::NCOL;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(sub * 32) << 16) + buf * C::NCOL + h * HALF;
 #pragma unroll
-      for (int cc = 0; cc < C::NCOL / 32; cc += 2) {
-        uint32_t v0[32], v1[32];
-        ptx::tmem_ld32(taddr + cc * 32, v0);
-        ptx::tmem_ld32(taddr + (cc + 1) * 32, v1);
+      for (int cc = 0; cc < HALF / 16; ++cc) {
+        uint32_t v[16];
+        ptx::tmem_ld16(taddr + cc * 16, v);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 w4 = reinterpret_cast<const float4*>(sW)[(cc + h) * 8 + j4];
-            const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = (cc + h) * 32 + j4 * 4 + e;
-              const int tt = col / HI, hj = col % HI;
-              const float x = __uint_as_float(h ? v1[j4 * 4 + e] : v0[j4 * 4 + e]);
-              acc[tt][hj % C::NACC] = fmaf(fmaxf(x, 0.f), wv[e], acc[tt][hj % C::NACC]);
-            }
-          }
+        for (int j = 0; j < 16; ++j) {
+          const int col = cc * 16 + j;
+          const int tt = col / HI, hj = col % HI;
+          acc[tt][hj % C::NACC] = fmaf(fmaxf(__uint_as_float(v[j]), 0.f), wr[col], acc[tt][hj % C::NACC]);
         }
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(t_empty(g));
+      if (lane == 0) ptx::mbar_arrive(t_empty(buf));
 #pragma unroll
-      for (int tt = 0; tt < C::TT; ++tt) {
+      for (int tt = 0; tt < TH; ++tt) {
         float sum = acc[tt][0];
 #pragma unroll
         for (int e = 1; e < C::NACC; ++e) sum += acc[tt][e];
-        const int r = row0 + tt;
+        const int r = row0 + h * TH + tt;
         if (kvalid && r < a.rows && s <= a.q_pos0 + r) {
           a.scores[static_cast<int64_t>(r) * a.ld + s] = sum * sk;
         }
