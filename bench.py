@@ -93,11 +93,11 @@ TRAFFIC_CAPTURES = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch over the last 1024 query rows of the 128K
     # prefill (each row against ~131K keys), per query row; the capture replays from a flushed L2, so
     # it overstates the steady state a little
-    "sparse_attn": {"src": "de17a35c046c29e4", "bytes_per_unit": (492.850e6 + 117.252e6) / 1024,
+    "sparse_attn": {"src": "3554cd61266f950e", "bytes_per_unit": (496.199e6 + 117.142e6) / 1024,
                     "capture": "ncu dram read + write, sparse_attn_kernel<0> over the 1024-row 128K tail, per row x rows"},
-    "indexer": {"src": "14cdd723e1ccffab", "bytes_per_unit": (63.560e6 + 475.289e6) / 1024,
+    "indexer": {"src": "4be8536f6d474e1b", "bytes_per_unit": (59.203e6 + 476.485e6) / 1024,
                 "capture": "ncu dram read + write, indexer_kernel<64> over the 1024-row 128K tail, per row x rows"},
-    "topk": {"src": "c8b05f44c8d040ca", "bytes_per_unit": (617.257e6 + 7.713e6) / 1024,
+    "topk": {"src": "04caa94b0b6fe425", "bytes_per_unit": (616.562e6 + 8.327e6) / 1024,
              "capture": "ncu dram read + write, topk_kernel over the 1024-row 128K tail, per row x rows"},
 }
 
