@@ -7,12 +7,12 @@
 // so the head-weighted ReLU sum for a (token, key) pair runs down one thread's registers with no
 // cross-thread reduction.  (The decode indexer over a paged cache is in indexer_paged.cu.)
 //
-// Warp roles (320 threads):
+// Warp roles (64 + 128 x NSPLIT threads: 576 for up to 64 heads, 320 for 128):
 //   warp 0      TMA producer: the query tile once, then key tiles through a ring of stages
 //   warp 1      owns TMEM and issues the FP8 MMAs (K = 128 as 4 x K32), one elected lane
-//   warps 2..9  epilogue: every tile's TMEM buffer is drained by all eight, warps w and w + 4
-//               splitting the columns of lanes [32*(w mod 4), +32); head weights in registers;
-//               ReLU, weight, sum over heads, key scale, causal mask, store fp32 scores.
+//   warps 2..   epilogue: every tile's TMEM buffer is drained by all of them, the NSPLIT warps
+//               that share a lane quarter (w mod 4) splitting its columns; head weights in
+//               registers; ReLU, weight, sum over heads, key scale, causal mask, store fp32 scores.
 #include "dsa_internal.h"
 #include "dsa_ptx.cuh"
 
@@ -22,7 +22,6 @@ namespace {
 constexpr int kTileKeys = 128;
 constexpr int kRowBytes = 128;  // d_I = 128 FP8 values per row
 constexpr int kKeyTileBytes = kTileKeys * kRowBytes;
-constexpr int kThreads = 320;
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 __host__ __device__ constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
@@ -32,6 +31,12 @@ struct IdxCfg {
   static constexpr int NCOL = 256;
   static constexpr int TT = NCOL / HI;
   static constexpr int NACC = (TT >= 32) ? 1 : ((32 / TT) < 4 ? (32 / TT) : 4);
+  // The epilogue splits the columns among NSPLIT warps per TMEM lane quarter: quarters of 64
+  // columns (whole tokens up to 64 heads), halves for 128 heads (a quarter would split a token).
+  static constexpr int NSPLIT = HI == 128 ? 2 : 4;
+  static constexpr int SPLIT = NCOL / NSPLIT;  // columns per epilogue thread
+  static constexpr int TS = TT / NSPLIT;       // tokens per split
+  static constexpr int THREADS = 64 + 128 * NSPLIT;
   static constexpr int STAGES = 6;
   static constexpr int Q_BYTES = NCOL * kRowBytes;
   static constexpr int TMEM_COLS = pow2_cols(2 * NCOL);
@@ -54,7 +59,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 }
 
 template <int HI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(IdxCfg<HI>::THREADS, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const IndexerArgs a) {
   using C = IdxCfg<HI>;
@@ -96,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(t_full(b), 1);
-      ptx::mbar_init(t_empty(b), 8);  // every epilogue warp drains every buffer
+      ptx::mbar_init(t_empty(b), 4 * C::NSPLIT);  // every epilogue warp drains every buffer
     }
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 2) {
     // w'[tt, j] = w[t, j] * q_scale[t, j]: ReLU is positively homogeneous, so the query
     // scale moves outside the ReLU and folds into the head weight.
-    for (int i = threadIdx.x - 64; i < C::NCOL; i += kThreads - 64) {
+    for (int i = threadIdx.x - 64; i < C::NCOL; i += C::THREADS - 64) {
       const int tt = i / HI, j = i % HI;
       const int r = row0 + tt;
       float v = 0.f;
@@ -179,14 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     drain_wait(mma_done, 0, a.limit_ns);
   } else {
     // ------------------------------------------------ epilogue
-    // Warps w and w + 4 share TMEM lanes [32*sub, 32*sub + 32) (sub = w mod 4) and split the
-    // columns: half h takes the (token, head) columns [128h, 128h + 128) of every tile, so each
-    // thread keeps the 128 head weights of its columns in registers for the whole block.  Read
+    // The NSPLIT warps that share TMEM lanes [32*sub, 32*sub + 32) (sub = w mod 4) split the
+    // columns: split h takes the (token, head) columns [SPLIT*h, SPLIT*h + SPLIT) of every tile, so
+    // each thread keeps the head weights of its columns in registers for the whole block.  Read
     // from shared memory for every tile instead (1 KB per thread per tile), the weights kept the
     // L1 data pipe 82% busy and set the kernel's time.  TMEM is read 16 columns at a time so that
-    // the weights, the columns and the sums fit in the 168 registers a thread has.
-    constexpr int HALF = C::NCOL / 2;
-    constexpr int TH = C::TT / 2;  // tokens per half
+    // the weights, the columns and the sums fit the registers a thread has.
+    constexpr int HALF = C::SPLIT;
+    constexpr int TH = C::TS;  // tokens per split
     const int h = (warp - 2) >> 2;
     const int sub = warp & 3;
     const int row = sub * 32 + lane;
@@ -269,7 +274,7 @@ cudaError_t launch_t(const CUtensorMap& qm, const CUtensorMap& km, int max_keys,
   auto kern = indexer_kernel<HI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(gx, gy), kThreads, C::SMEM, stream>>>(qm, km, a);
+  kern<<<dim3(gx, gy), C::THREADS, C::SMEM, stream>>>(qm, km, a);
   return cudaGetLastError();
 }
 
