@@ -95,7 +95,7 @@ TRAFFIC_CAPTURES = {
     # it overstates the steady state a little
     "sparse_attn": {"src": "3554cd61266f950e", "bytes_per_unit": (496.199e6 + 117.142e6) / 1024,
                     "capture": "ncu dram read + write, sparse_attn_kernel<0> over the 1024-row 128K tail, per row x rows"},
-    "indexer": {"src": "4be8536f6d474e1b", "bytes_per_unit": (59.203e6 + 476.485e6) / 1024,
+    "indexer": {"src": "1e33e0a7572a36a2", "bytes_per_unit": (63.660e6 + 477.555e6) / 1024,
                 "capture": "ncu dram read + write, indexer_kernel<64> over the 1024-row 128K tail, per row x rows"},
     "topk": {"src": "04caa94b0b6fe425", "bytes_per_unit": (616.562e6 + 8.327e6) / 1024,
              "capture": "ncu dram read + write, topk_kernel over the 1024-row 128K tail, per row x rows"},
