@@ -88,8 +88,10 @@ __device__ void select_bin(TopkSmem& s, int nbins, uint32_t kk) {
   __syncthreads();
 }
 
-// Three-level radix select over keys visited by `each(f)` (f(key) per key): returns the key
-// thr of the rank-th largest and how many keys equal to thr belong to the top `rank`.
+// Three-level radix select over keys visited by `each(f)` (f(key) per key): returns a key thr and
+// a count n_equal such that the top `rank` are the keys > thr plus n_equal of the keys == thr
+// (thr is the rank-th largest key, or, when a coarser bin already splits the set exactly, the key
+// just below that bin with n_equal = 0).
 // With kLevels == 2 the last 8 key bits are left open: thr is the lowest key of the 24-bit prefix
 // that holds the rank-th largest key (a lower bound of it) and n_equal is not set.
 template <int kLevels = 3, class Each>
@@ -102,7 +104,18 @@ __device__ void radix_threshold(TopkSmem& s, uint32_t rank, Each&& each, uint32_
   select_bin(s, kBins, rank);
   const uint32_t top = s.sel_bin;
   uint32_t need = rank - s.sel_above;
+  const uint32_t in_top = s.hist[top];
   __syncthreads();
+  // Exact selection: when the bin that holds the rank-th key holds exactly the keys still needed,
+  // every key of it is selected and no finer level is needed (thr just below the bin, no ties).
+  // (Block-uniform: every thread read the same counts.)
+  if constexpr (kLevels == 3) {
+    if (in_top == need && top != 0) {
+      *thr = (top << 20) - 1;
+      *n_equal = 0;
+      return;
+    }
+  }
   for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
   __syncthreads();
   each([&](uint32_t key) {
@@ -112,10 +125,16 @@ __device__ void radix_threshold(TopkSmem& s, uint32_t rank, Each&& each, uint32_
   select_bin(s, kBins, need);
   const uint32_t pre24 = (top << 12) | s.sel_bin;
   need -= s.sel_above;
+  const uint32_t in_pre24 = s.hist[s.sel_bin];
   __syncthreads();
   if constexpr (kLevels == 2) {
     *thr = pre24 << 8;
   } else {
+    if (in_pre24 == need && pre24 != 0) {
+      *thr = (pre24 << 8) - 1;
+      *n_equal = 0;
+      return;
+    }
     for (int b = tid; b < 256; b += kThreads) s.hist[b] = 0;
     __syncthreads();
     each([&](uint32_t key) {
