@@ -777,14 +777,7 @@ def bench_decode(dsa, synth, args, peaks, cid=5):
         stages({"index": [], "topk": [], "attn": []})
     # the step as a serving loop runs it: the dsa_forward call (four launches) captured once into a
     # CUDA graph and replayed, so that no launch gap sits between its kernels
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        f()
-    torch.cuda.current_stream().wait_stream(side)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        f()
+    graph = f.capture()
     for _ in range(max(3, args.warmup)):
         graph.replay()
     n = max(10, args.steps)

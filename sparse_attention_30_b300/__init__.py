@@ -355,6 +355,22 @@ class Forward:
         """Device-side status of the calls made with this workspace since the last read (dsa_status)."""
         return read_status(self.ws, stream)
 
+    def capture(self):
+        """One call captured into a CUDA graph (a torch.cuda.CUDAGraph): graph.replay() runs the same
+        launches on the same buffers with no per-launch host work, as a serving loop runs its decode
+        step.  The inputs are read when the graph replays, so a step writes its new tokens into the
+        same tensors before replaying.  The status word keeps collecting the replays' errors."""
+        dev = self.ws.device
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self()  # one call outside the capture (first-use kernel attributes are set here)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self()
+        return graph
+
 
 LOSS_SPARSE, LOSS_DENSE_WARMUP = 0, 1
 

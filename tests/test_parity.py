@@ -560,6 +560,36 @@ def test_forward_decode_full_config(dsa, cid):
         _check_row(hinp, b, cfg.k, cfg.scale, idx[b], out[b], lse[b], decode=True, where=f"cfg{cid}")
 
 
+def test_forward_decode_graph_replay_matches_the_call(dsa):
+    """The decode step captured into a CUDA graph (Forward.capture) and replayed selects the eager
+    call's sets (output slots are filled in no fixed order) and reports through the same status
+    word; its outputs pass the oracle check.  (Two calls need not agree bit for bit: the online
+    softmax rounds P to bf16 against the running maximum of the slots seen so far, and the slot
+    order differs from call to call.)"""
+    cfg = synth.config(5)
+    d = synth.decode_inputs(cfg, device="cuda")
+    max_len = int(d["seq_lens"].max())
+    idx = torch.empty((cfg.B, cfg.k), dtype=torch.int32, device="cuda")
+    lse = torch.empty((cfg.B, cfg.H), dtype=torch.float32, device="cuda")
+    f = dsa.Forward.decode(d, cfg.k, cfg.scale, max_len, idx=idx, lse=lse)
+    f()
+    torch.cuda.synchronize()
+    ref_idx = idx.clone()
+    graph = f.capture()
+    hinp = _host(d)
+    for rep in range(2):
+        idx.fill_(-7)
+        f.out.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert f.status() == 0 and dsa.device_status() == 0
+        assert torch.equal(torch.sort(idx, dim=1).values, torch.sort(ref_idx, dim=1).values)
+        i_h, o_h, l_h = idx.cpu().numpy(), f.out.float().cpu().numpy(), lse.cpu().numpy()
+        for b in ([0, 13, cfg.B - 1] if rep == 0 else [6]):
+            _check_row(hinp, b, cfg.k, cfg.scale, i_h[b], o_h[b], l_h[b], decode=True, where="graph replay")
+
+
 def test_forward_decode_small_batch_splits_keys(dsa):
     # two sequences: the driver spreads each sequence's selected keys over four clusters and merges
     cfg = synth.config(5, B=2, ctx_lo=3000, ctx_hi=9000, seed=9)
