@@ -502,7 +502,9 @@ def test_forward_prefill_config2_sampled_rows(dsa):
     idx, out, lse = f.idx.cpu().numpy(), f.out.float().cpu().numpy(), f.lse.cpu().numpy()
     rows = sorted(set([0, 1, 2, 3, 999, 1000, 2046, 2047, 2048, 2049, 4094, 4095] + list(range(5, 4096, 61))))
     swaps = sum(_check_row(hinp, t, cfg.k, cfg.scale, idx[t], out[t], lse[t], where="cfg2") for t in rows)
-    assert swaps <= len(rows)  # near-tie swaps are rare
+    # positions in one set but not the other (two per near-tie swap): 0 observed over these 80 rows
+    # on a B300; at most one swap is allowed in the whole sample
+    assert swaps <= 2, swaps
 
 
 def test_forward_prefill_chunked_selection_matches_the_separate_calls(dsa):
