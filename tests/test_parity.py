@@ -592,6 +592,26 @@ def test_forward_decode_graph_replay_matches_the_call(dsa):
             _check_row(hinp, b, cfg.k, cfg.scale, i_h[b], o_h[b], l_h[b], decode=True, where="graph replay")
 
 
+def test_forward_prefill_graph_replay_against_oracle(dsa):
+    """A chunked prefill (three 100-row chunks) captured into a CUDA graph and replayed: every row's
+    selection and attention pass the oracle check, and the status word stays clear."""
+    cfg = synth.config(1)
+    hinp = synth.prefill_inputs(cfg)
+    d = _cuda(hinp)
+    idx = torch.empty((cfg.L, cfg.k), dtype=torch.int32, device="cuda")
+    lse = torch.empty((cfg.L, cfg.H), dtype=torch.float32, device="cuda")
+    f = dsa.Forward.prefill(d, cfg.k, cfg.scale, chunk_rows=100, lse=lse, idx=idx)
+    graph = f.capture()
+    idx.fill_(-7)
+    f.out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert f.status() == 0 and dsa.device_status() == 0
+    i_h, o_h, l_h = idx.cpu().numpy(), f.out.float().cpu().numpy(), lse.cpu().numpy()
+    for t in range(cfg.L):
+        _check_row(hinp, t, cfg.k, cfg.scale, i_h[t], o_h[t], l_h[t], where="prefill graph replay")
+
+
 def test_forward_decode_small_batch_splits_keys(dsa):
     # two sequences: the driver spreads each sequence's selected keys over four clusters and merges
     cfg = synth.config(5, B=2, ctx_lo=3000, ctx_hi=9000, seed=9)
