@@ -97,7 +97,7 @@ TRAFFIC_CAPTURES = {
                     "capture": "ncu dram read + write, sparse_attn_kernel<0> over the 1024-row 128K tail, per row x rows"},
     "indexer": {"src": "1e33e0a7572a36a2", "bytes_per_unit": (63.660e6 + 477.555e6) / 1024,
                 "capture": "ncu dram read + write, indexer_kernel<64> over the 1024-row 128K tail, per row x rows"},
-    "topk": {"src": "04caa94b0b6fe425", "bytes_per_unit": (616.562e6 + 8.327e6) / 1024,
+    "topk": {"src": "dca55ab2c805bc87", "bytes_per_unit": (616.624e6 + 8.071e6) / 1024,
              "capture": "ncu dram read + write, topk_kernel over the 1024-row 128K tail, per row x rows"},
 }
 
